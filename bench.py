@@ -1,0 +1,542 @@
+#!/usr/bin/env python
+"""Benchmark of the bitmask N:M decode SpMV on one decode token's linear stack.
+
+A step is one decode token through every pruned linear of a Llama-3.1-8B-shaped
+model: 32 layers x {qkv 6144x4096, o 4096x4096, gate_up 28672x4096,
+down 4096x14336}, batch 1, pattern 2:4, i.e. 128 nm_spmv launches chained with
+programmatic dependent launch and replayed as one CUDA graph. Weights are
+synthetic (bf16 N(0, 0.02^2), Wanda-selected with a synthetic column norm,
+packed on the GPU); the step reads 7.85 GB, far more than L2, so no flush is
+needed between steps.
+
+Prints one JSON line. ``value`` is microseconds per decode token (lower is
+better) over the whole job. Extra keys: the same-GPU dense references (the
+hand-written dense GEMV and cuBLAS), the roofline of the SpMV kernel, the CPU
+oracle as a timed baseline, an end-to-end figure with host buffers, and the SM
+clocks seen during the timed region.
+
+``--impl reference`` times the CPU oracle instead (the only reference
+implementation this method has), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "bitmask N:M SpMV µs/decode-token (8B shapes), HBM GB/s vs peak, × vs dense GEMV"
+UNIT = "us/token"
+CONFIG_ID = 2  # stream-id namespace of the decode-token stack inputs
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "nm_spmv_llama8b_stack.txt")
+SPMV_SOURCE = os.path.join(ROOT, "sparse_decoding_gb300", "csrc", "spmv.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--model", default="llama3.1-8b", choices=sorted(synth.MODELS))
+    ap.add_argument("--pattern", default="2:4")
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (0 = the model's)")
+    ap.add_argument("--no-variants", action="store_true", help="skip the extra pattern/batch lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def parse_pattern(s: str):
+    n, m = s.split(":")
+    return int(n), int(m)
+
+
+# --- multi-process (one process per GPU; replicas) ------------------------------------
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    """Max of a per-rank float over all ranks (the job is as slow as its slowest rank)."""
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --- bytes -------------------------------------------------------------------------------
+
+def sparse_bytes(rows, K, batch):
+    """Algorithmic bytes of one SpMV: kept values + masks + x + bf16 y."""
+    return rows * (K // 2 * 2 + K // 8) + batch * K * 2 + batch * rows * 2
+
+
+def dense_bytes(rows, K, batch):
+    return rows * K * 2 + batch * K * 2 + batch * rows * 2
+
+
+# --- clocks (NVML through ctypes; reading only) --------------------------------------------
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons of this process's GPU every ~2 ms."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int):
+        self.ok = False
+        self.samples = []
+        self.max_mhz = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+        self._stop = threading.Event()
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0 and \
+                    self._reasons(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((mhz.value, rs.value))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
+
+
+# --- workload ---------------------------------------------------------------------------------
+
+class Stack:
+    """All linears of one decode token: weights packed per pattern, x/y per batch size."""
+
+    def __init__(self, nm, model: str, patterns, batches, layers: int, keep_dense: bool, seed: int = 0):
+        shapes = synth.MODELS[model]
+        self.model = model
+        self.layers = layers or shapes["layers"]
+        self.shapes = [(name, shapes[name][0], shapes[name][1]) for name in synth.MATRICES]
+        self.packed = {p: [] for p in patterns}
+        self.dense = []
+        for layer in range(self.layers):
+            for mi, (name, rows, K) in enumerate(self.shapes):
+                W = synth.weights(rows, K, seed, synth.stream_id(CONFIG_ID, layer, mi, 0), device="cuda")
+                a = synth.col_norms(K, seed, synth.stream_id(CONFIG_ID, layer, mi, 1), device="cuda")
+                for pi, (N, M) in enumerate(patterns):
+                    Wp = nm.select(W, a, N, M)
+                    self.packed[(N, M)].append(nm.pack(Wp, N, M))
+                    if keep_dense and pi == 0:
+                        self.dense.append(Wp)
+                    else:
+                        del Wp
+                del W, a
+        self.io = {}
+        for b in batches:
+            ktot = sum(K for _, _, K in self.shapes) * self.layers
+            rtot = sum(r for _, r, _ in self.shapes) * self.layers
+            x_all = torch.empty(b * ktot, dtype=torch.bfloat16, device="cuda")
+            y_all = torch.empty(b * rtot, dtype=torch.bfloat16, device="cuda")
+            xs, ys = [], []
+            xo = yo = 0
+            for layer in range(self.layers):
+                for mi, (name, rows, K) in enumerate(self.shapes):
+                    x = x_all[xo:xo + b * K].view(b, K)
+                    x.copy_(synth.activations(b, K, seed, synth.stream_id(CONFIG_ID, layer, mi, 2), device="cuda"))
+                    xs.append(x)
+                    ys.append(y_all[yo:yo + b * rows].view(b, rows))
+                    xo += b * K
+                    yo += b * rows
+            self.io[b] = (x_all, y_all, xs, ys)
+        torch.cuda.synchronize()
+
+    def linears(self):
+        for layer in range(self.layers):
+            for name, rows, K in self.shapes:
+                yield name, rows, K
+
+    def sparse_ops(self, pattern, batch, only=None):
+        _, _, xs, ys = self.io[batch]
+        ops = []
+        for i, (name, rows, K) in enumerate(self.linears()):
+            if only and name != only:
+                continue
+            m, v = self.packed[pattern][i]
+            ops.append(dict(masks=m, values=v, x=xs[i], y=ys[i], rows=rows, K=K))
+        return ops
+
+    def dense_ops(self, batch):
+        _, _, xs, ys = self.io[batch]
+        return [dict(W=self.dense[i], x=xs[i], y=ys[i], rows=rows, K=K)
+                for i, (name, rows, K) in enumerate(self.linears())]
+
+    def bytes(self, batch, dense=False, only=None):
+        f = dense_bytes if dense else sparse_bytes
+        return sum(f(rows, K, batch) for name, rows, K in self.linears() if not only or name == only)
+
+
+def capture(fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps, warmup, world=1, sampler=None):
+    """Device time of `steps` replays (CUDA events on the replay stream); returns (mean_ms, median_ms)."""
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        ev[0].record()
+        for i in range(steps):
+            g.replay()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+    barrier(world)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]) / steps, statistics.median(per)
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """dram bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    try:
+        fields = {}
+        for line in open(PROFILE_SUMMARY):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(SPMV_SOURCE, "rb").read()).hexdigest()
+        if fields.get("kernel_source_sha256") != sha:
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# --- CPU oracle baseline -------------------------------------------------------------------------
+
+def _bits(t: torch.Tensor):
+    import numpy as np
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def build_oracle_sample(model, N, M, batch, row_frac, seed=0):
+    import oracle
+    shapes = synth.MODELS[model]
+    sample = []
+    for mi, name in enumerate(synth.MATRICES):
+        rows, K = shapes[name]
+        r = max(32, int(rows * row_frac))
+        W = _bits(synth.weights(r, K, seed, synth.stream_id(CONFIG_ID, 0, mi, 0)))
+        a = synth.col_norms(K, seed, synth.stream_id(CONFIG_ID, 0, mi, 1)).numpy()
+        masks, values = oracle.pack(oracle.select(W, a, N, M), N, M)
+        x = _bits(synth.activations(batch, K, seed, synth.stream_id(CONFIG_ID, 0, mi, 2)))
+        sample.append((name, rows, r, K, masks, values, x))
+    return sample
+
+
+def time_oracle_token(sample, layers):
+    """One oracle pass over the sample; returns (seconds, estimated seconds per decode token)."""
+    import oracle
+    t_sample = 0.0
+    t_token = 0.0
+    for name, rows, r, K, masks, values, x in sample:
+        t0 = time.perf_counter()
+        oracle.spmv_packed_f64(masks, values, x, K)
+        dt = time.perf_counter() - t0
+        t_sample += dt
+        t_token += dt * (rows / r) * layers
+    return t_sample, t_token
+
+
+def sample_desc(sample, layers, N, M, batch):
+    parts = ", ".join(f"{name} {r}/{rows} rows x K={K}" for name, rows, r, K, *_ in sample)
+    return (f"oracle (plain C, fp64, decode + dense product, 1 thread) on layer 0 of the stack: {parts}; "
+            f"{N}:{M}, batch {batch}; time scaled by rows and by {layers} layers to one decode token")
+
+
+def cpu_cores_available():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# --- arms -------------------------------------------------------------------------------------------
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step one bounded sample of the decode-token stack."""
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return
+    N, M = parse_pattern(args.pattern)
+    layers = args.layers or synth.MODELS[args.model]["layers"]
+    sample = build_oracle_sample(args.model, N, M, args.batch, row_frac=1 / 64)
+    for _ in range(args.warmup):
+        time_oracle_token(sample, layers)
+    tokens = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        _, t_tok = time_oracle_token(sample, layers)
+        tokens.append(t_tok)
+    wall = time.perf_counter() - t_all
+    us = statistics.mean(tokens) * 1e6
+    desc = sample_desc(sample, layers, N, M, args.batch)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(args.model, N, M, args.batch, layers),
+        "cpu_baseline": {"kind": "oracle", "value": us, "unit": UNIT, "cores": 1, "sample": desc},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def workload_config(model, N, M, batch, layers):
+    shapes = synth.MODELS[model]
+    lin = ", ".join(f"{n} {shapes[n][0]}x{shapes[n][1]}" for n in synth.MATRICES)
+    return {"workload": f"{model}-shaped decode-token linear stack: {layers} layers x ({lin}), "
+                        f"{N}:{M}, batch {batch}",
+            "pattern": f"{N}:{M}", "batch": batch, "layers": layers, "launches_per_step": 4 * layers,
+            "l2": "inputs larger than L2 (every step streams all weights of all layers)",
+            "weights": "bf16 N(0,0.02^2), Wanda N:M selection with a=|N(1,0.3^2)|, packed on the GPU",
+            "x": "bf16 N(0,1), independent per linear", "launch": "CUDA graph of PDL-chained launches"}
+
+
+def run_ours(args):
+    rank, world, local = dist_init()
+    torch.cuda.set_device(local)
+    import sparse_decoding_gb300 as nm
+    nm.init()
+    N, M = parse_pattern(args.pattern)
+    head = (N, M)
+    patterns = [head]
+    if not args.no_variants:
+        alt = (16, 32) if head != (16, 32) else (2, 4)
+        patterns.append(alt)
+    batches = [args.batch] + ([] if args.no_variants or args.batch == 4 else [4])
+    stack = Stack(nm, args.model, patterns, batches, args.layers, keep_dense=True)
+    layers = stack.layers
+    B = args.batch
+
+    # headline: the sparse stack, one decode token per replay
+    sparse_plan = stack.sparse_ops(head, B)
+    g_sparse = capture(lambda: nm.spmv_stack(sparse_plan, B))
+    sampler = ClockSampler(local)
+    ms_mean, ms_med = time_graph(g_sparse, args.steps, args.warmup, world, sampler)
+    ms_max = max_over_ranks(ms_mean, world)
+    value = ms_max * 1e3 / world  # us per token over the whole job (replicas)
+
+    step_bytes = stack.bytes(B)
+    achieved = step_bytes / (ms_mean * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # dense references: the hand-written GEMV and cuBLAS, same graph discipline
+    dense_plan = stack.dense_ops(B)
+    g_dense = capture(lambda: nm.dense_gemv_stack(dense_plan, B))
+    dense_ms, _ = time_graph(g_dense, args.steps, args.warmup, world)
+
+    def cublas_stack():
+        for op in dense_plan:
+            torch.mm(op["x"], op["W"].t(), out=op["y"])
+    g_cublas = capture(cublas_stack)
+    cublas_ms, _ = time_graph(g_cublas, args.steps, args.warmup, world)
+    best_dense = min(dense_ms, cublas_ms)
+
+    # per-shape kernel bandwidth (each graph launches one shape across all layers)
+    per_shape = {}
+    for name, rows, K in stack.shapes:
+        ops = stack.sparse_ops(head, B, only=name)
+        g = capture(lambda ops=ops: nm.spmv_stack(ops, B))
+        t, _ = time_graph(g, max(5, args.steps // 5), 3, world)
+        per_launch_us = t * 1e3 / len(ops)
+        per_shape[name] = {"rows": rows, "K": K, "us_per_launch": round(per_launch_us, 3),
+                           "GB_s": round(sparse_bytes(rows, K, B) / (per_launch_us * 1e-6) / 1e9, 1)}
+        del g
+
+    variants = {}
+    if not args.no_variants:
+        for (pat, b) in [(patterns[-1], B)] + ([(head, 4)] if 4 in stack.io and B != 4 else []):
+            ops = stack.sparse_ops(pat, b)
+            g = capture(lambda ops=ops, b=b: nm.spmv_stack(ops, b))
+            t, _ = time_graph(g, args.steps, min(args.warmup, 10), world)
+            by = stack.bytes(b)
+            variants[f"{pat[0]}:{pat[1]} batch {b}"] = {
+                "us_per_token": round(t * 1e3, 2), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
+                "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4)}
+            del g
+
+    # end to end through the public API: pinned host x in, stack, host y out, every step
+    x_all, y_all, _, _ = stack.io[B]
+    x_host = torch.empty(x_all.shape, dtype=x_all.dtype, pin_memory=True)
+    x_host.copy_(x_all)
+    y_host = torch.empty(y_all.shape, dtype=y_all.dtype, pin_memory=True)
+    plan = nm.StackPlan(sparse_plan, B)
+
+    def e2e_step():
+        x_all.copy_(x_host, non_blocking=True)
+        plan.run()
+        y_host.copy_(y_all, non_blocking=True)
+    for _ in range(min(args.warmup, 10)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_wall = (time.perf_counter() - t0) / args.steps * 1e3
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1) / args.steps, e2e_wall), world)
+
+    status = nm.device_status()
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "median_ms_per_step": round(ms_med, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(args.model, N, M, B, layers),
+        "hbm_GB_s": round(achieved, 1),
+        "x_vs_dense": {"hand_written_dense_us": round(dense_ms * 1e3, 2), "cublas_dense_us": round(cublas_ms * 1e3, 2),
+                       "ratio_vs_best_dense": round(best_dense / ms_mean, 4),
+                       "dense_GB_s": round(stack.bytes(B, dense=True) / (dense_ms * 1e-3) / 1e9, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": recorded_traffic(),
+                     "kernel": "spmv_tma_kernel",
+                     "achieved_basis": f"{step_bytes} algorithmic bytes per step / {4 * layers} launches, "
+                                       "over the event-timed step (gaps between launches included)"},
+        "per_shape": per_shape,
+        "variants": variants,
+        "e2e": {"value": round(e2e_ms * 1e3 / world, 3), "unit": UNIT,
+                "h2d_bytes_per_step": x_all.numel() * 2, "d2h_bytes_per_step": y_all.numel() * 2,
+                "path": "pinned host x -> device, nm_spmv_stack through the C ABI (no graph), y -> pinned host"},
+        "gpu_launches": 4 * layers * args.steps,
+        "clocks": sampler.summary(),
+        "device_status": nm.status_str(status),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = build_oracle_sample(args.model, N, M, B, row_frac=1 / 8)
+        ts = []
+        t_all = time.perf_counter()
+        while True:
+            t_sample, t_tok = time_oracle_token(sample, layers)
+            ts.append(t_tok)
+            if len(ts) >= 3 or time.perf_counter() - t_all > 20:
+                break
+        out["cpu_baseline"] = {"value": round(statistics.median(ts) * 1e6, 1), "unit": UNIT, "cores": 1,
+                               "kind": "oracle", "sample": sample_desc(sample, layers, N, M, B),
+                               "host_cores_available": cpu_cores_available(), "repeats": len(ts)}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * nmspmv.h -- C ABI of the GB300 (sm_103a) bitmask N:M decode SpMV library.
+ *
+ * The operation is the decode-time sparse matrix-vector product of
+ * SparseDecoding ("Decoding-Aware Pruning for Accurate and Efficient LLM
+ * Inference"): weights pruned to a 50% N:M pattern are stored row by row as
+ * 32-bit bitmasks plus the kept values, and each decode step multiplies them
+ * with the current token's activations (paper.rainbus.top summary, section
+ * "方法步骤详情", steps 3-4; ai.info summary, "Methodology in Plain English",
+ * steps 2-3).
+ *
+ * Storage format (the ABI format):
+ *   masks  : uint32 [rows][K/32], row-major. Bit j (LSB = 0) of word g of row r
+ *            is set when column 32g+j is kept.
+ *   values : bf16   [rows][K/2],  row-major. values[r][16g+k] is the k-th kept
+ *            weight of word g, counting set bits from the LSB (ascending
+ *            column order). Every word has exactly 16 set bits.
+ *   x      : bf16   [batch][K],   one contiguous row per token.
+ *   y      : bf16 (or fp32) [batch][rows].
+ *
+ * Conventions for every call below:
+ *   - bf16 data is passed as raw 16-bit patterns (uint16_t / void *).
+ *   - Device pointers are caller-owned device memory; the library never frees
+ *     them. Host pointers are caller-owned host memory.
+ *   - Every pointer that the call reads or writes must be 16-byte aligned
+ *     (NM_ERR_ALIGN otherwise). Pointers may be NULL only when the call has
+ *     nothing to read or write through them (rows == 0).
+ *   - K must be a multiple of 32 (NM_ERR_SHAPE). rows, K >= 0.
+ *   - (N, M) must be one of (2,4), (4,8), (8,16), (16,32) (NM_ERR_UNSUPPORTED):
+ *     the 50% patterns with M <= 32 dividing the word.
+ *   - batch must be 1..8 (NM_ERR_UNSUPPORTED).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Device calls
+ *     are asynchronous on it unless stated otherwise.
+ *   - A failed CUDA call or launch returns NM_ERR_CUDA. No kernel spin-waits
+ *     without a bound: a bounded wait that runs out records NM_ERR_TIMEOUT in
+ *     a per-device status word that nm_device_status() reports.
+ *   - The library keeps one small scratch buffer per device (the stream-K
+ *     partial sums and their counters, and the pack error flag). It is
+ *     allocated by the first call on that device that needs it and kept until
+ *     the process exits; make that first call outside CUDA graph capture.
+ *     Calls that use it must not run concurrently on different streams of the
+ *     same device.
+ */
+#ifndef NMSPMV_H
+#define NMSPMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nm_status {
+    NM_OK = 0,
+    NM_ERR_INVALID_ARG = 1, /* NULL where data is needed, bad count */
+    NM_ERR_SHAPE = 2,       /* K % 32 != 0, negative size */
+    NM_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    NM_ERR_UNSUPPORTED = 4, /* (N, M) not a 50% pattern, batch outside 1..8 */
+    NM_ERR_NOT_NM = 5,      /* an M-subgroup holds more than N nonzeros */
+    NM_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+    NM_ERR_TIMEOUT = 7      /* a kernel's bounded wait ran out */
+} nm_status;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int nm_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *nm_status_str(int status);
+
+/*
+ * nm_pack_host -- bitmask conversion on the host (paper.rainbus.top summary,
+ * "方法步骤详情" step 3: each pruned row becomes a compact value array plus
+ * 32-bit bitmasks whose set bits mark the kept weights).
+ *   W_bf16 : host, bf16 [rows][K], the pruned dense matrix (read).
+ *   masks  : host, uint32 [rows][K/32] (written).
+ *   values : host, bf16 [rows][K/2] (written).
+ * A weight is kept when it is nonzero (+0 and -0 count as zero; NaN and Inf
+ * as nonzero). An M-subgroup with fewer than N nonzeros is filled up to N with
+ * its lowest-index zero positions; kept values are copied bit for bit.
+ * Returns NM_ERR_NOT_NM when an aligned M-subgroup holds more than N
+ * nonzeros (outputs then unspecified). Synchronous, no CUDA.
+ */
+nm_status nm_pack_host(const uint16_t *W_bf16, int64_t rows, int64_t K, int N, int M,
+                       uint32_t *masks, uint16_t *values);
+
+/*
+ * nm_select -- Wanda N:M selection on the GPU (daiwk.github.io notes,
+ * section "核心公式": score s_ij = |W_ij| * sqrt(sum_t X_jt^2), keep N per
+ * M-column group, no weight update).
+ *   W_bf16   : device, bf16 [rows][K] (read).
+ *   a        : device, fp32 [K], the per-column activation norm (read).
+ *   W_pruned : device, bf16 [rows][K] (written); may equal W_bf16 (in place).
+ * In every aligned M-column subgroup of every row the N entries with the
+ * largest fp32 score |W| * a_j are kept (bit for bit) and the others become
+ * +0. Larger score wins; a NaN score counts as larger than any number; equal
+ * scores go to the lower column index. Asynchronous.
+ */
+nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M,
+                    void *W_pruned, void *stream);
+
+/*
+ * nm_pack -- bitmask conversion on the GPU, bit-exact with nm_pack_host.
+ *   W_bf16 : device, bf16 [rows][K] (read). masks, values_bf16: device (written).
+ * Synchronous with respect to `stream`: it waits for the stream so that it can
+ * report NM_ERR_NOT_NM. Uses the per-device scratch (error flag).
+ */
+nm_status nm_pack(const void *W_bf16, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
+                  void *values_bf16, void *stream);
+
+/*
+ * nm_spmv -- decode SpMV over the bitmask format (paper.rainbus.top summary,
+ * "核心方法" and "方法步骤详情" step 4; ai.info summary, "Methodology in Plain
+ * English" step 3): for each mask word, 16 fixed steps each take the next set
+ * bit as the column of the next kept value and multiply-accumulate.
+ *   y[b][r] = sum_j W[r][j] * x[b][j] for b < batch, accumulated in fp32 and
+ *   rounded to bf16 (nearest even).
+ *   masks, values_bf16, x_bf16: device (read). y_bf16: device (written).
+ * Masks are not validated: on words that do not hold exactly 16 set bits, y is
+ * unspecified but no access leaves the caller's buffers. The summation order
+ * is fixed for a given device and shape (the result is repeatable).
+ * Asynchronous. Uses the per-device scratch (stream-K partial sums).
+ */
+nm_status nm_spmv(const uint32_t *masks, const void *values_bf16, const void *x_bf16,
+                  void *y_bf16, int64_t rows, int64_t K, int batch, void *stream);
+
+/* As nm_spmv, but y is the fp32 accumulator before rounding: float [batch][rows]. */
+nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const void *x_bf16,
+                         float *y_f32, int64_t rows, int64_t K, int batch, void *stream);
+
+/*
+ * dense_gemv -- the dense bf16 reference on the same GPU (the pages' 1.00x
+ * baseline: aitest123.com article, Table 3; ai.info summary, Main Findings).
+ *   W_bf16: device bf16 [rows][K]; x_bf16: device bf16 [batch][K];
+ *   y: device bf16 [batch][rows] (fp32 accumulation, rounded to nearest even).
+ * Asynchronous.
+ */
+nm_status dense_gemv(const void *W_bf16, const void *x_bf16, void *y_bf16, int64_t rows,
+                     int64_t K, int batch, void *stream);
+
+/* As dense_gemv with the fp32 accumulator as output: float [batch][rows]. */
+nm_status dense_gemv_f32out(const void *W_bf16, const void *x_bf16, float *y_f32, int64_t rows,
+                            int64_t K, int batch, void *stream);
+
+/*
+ * One linear of a decode-token stack. `W` is the dense bf16 matrix for the
+ * dense stack and unused (may be NULL) for the sparse one; `masks`/`values`
+ * are the packed form for the sparse stack and unused for the dense one.
+ */
+typedef struct nm_linear {
+    const uint32_t *masks;
+    const void *values; /* bf16 [rows][K/2] */
+    const void *W;      /* bf16 [rows][K] */
+    const void *x;      /* bf16 [batch][K] */
+    void *y;            /* bf16 [batch][rows] */
+    int64_t rows;
+    int64_t K;
+} nm_linear;
+
+/*
+ * nm_spmv_stack / dense_gemv_stack -- the linear stack of one decode token
+ * (every pruned linear of every layer; only linear layers are sparse, per the
+ * ai.info summary, "Methodology" step 4 and paper.rainbus.top "局限与改进").
+ * Runs ops[0..n_ops) in order on `stream`, each as nm_spmv / dense_gemv.
+ * Consecutive launches are chained with programmatic dependent launch: a
+ * kernel may start streaming its own weights before the previous one ends,
+ * but reads its x only after the previous kernel has completed, exactly as if
+ * x were that kernel's output. `ops` is host memory, read during the call.
+ * The sequence may be captured into a CUDA graph by the caller.
+ */
+nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
+nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
+
+/*
+ * nm_device_status -- waits for `stream`, then returns and clears the status
+ * word of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
+ * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed).
+ */
+nm_status nm_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NMSPMV_H */

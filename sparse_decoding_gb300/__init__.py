@@ -1,0 +1,232 @@
+"""GB300-native bitmask N:M decode SpMV (the decode kernel of SparseDecoding).
+
+This package is a thin ctypes binding over ``libnmspmv.so`` (C ABI in
+``include/nmspmv.h``). Every step of the computation runs in the library's
+CUDA kernels; this module only checks tensor types and passes pointers, sizes
+and the current CUDA stream. PyTorch supplies device memory and streams.
+
+There is no fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnmspmv.so")
+
+NM_OK = 0
+NM_ERR_INVALID_ARG = 1
+NM_ERR_SHAPE = 2
+NM_ERR_ALIGN = 3
+NM_ERR_UNSUPPORTED = 4
+NM_ERR_NOT_NM = 5
+NM_ERR_CUDA = 6
+NM_ERR_TIMEOUT = 7
+
+PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
+
+# Every symbol the header declares (the CPU test checks they are exported).
+EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
+           "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
+           "nm_device_status")
+
+
+class NmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+class NmLinear(ctypes.Structure):
+    """Mirror of ``nm_linear`` in include/nmspmv.h."""
+    _fields_ = [("masks", ctypes.c_void_p), ("values", ctypes.c_void_p), ("W", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("K", ctypes.c_int64)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libnmspmv.so (built by ``sparse_decoding_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -m sparse_decoding_gb300.build` "
+                           "(or __graft_entry__.build()) first")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    sig = {
+        "nm_abi_version": ([], i32),
+        "nm_status_str": ([i32], ctypes.c_char_p),
+        "nm_pack_host": ([p, i64, i64, i32, i32, p, p], i32),
+        "nm_select": ([p, p, i64, i64, i32, i32, p, p], i32),
+        "nm_pack": ([p, i64, i64, i32, i32, p, p, p], i32),
+        "nm_spmv": ([p, p, p, p, i64, i64, i32, p], i32),
+        "nm_spmv_f32out": ([p, p, p, p, i64, i64, i32, p], i32),
+        "dense_gemv": ([p, p, p, i64, i64, i32, p], i32),
+        "dense_gemv_f32out": ([p, p, p, i64, i64, i32, p], i32),
+        "nm_spmv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
+        "dense_gemv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
+        "nm_device_status": ([p], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = L
+    return L
+
+
+def status_str(status: int) -> str:
+    return lib().nm_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != NM_OK:
+        raise NmError(status, where)
+
+
+def _stream(t: Optional[torch.Tensor] = None) -> int:
+    dev = t.device if t is not None else None
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _cuda(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise TypeError(f"{name} must be contiguous")
+    return t
+
+
+def _x2d(x: torch.Tensor) -> torch.Tensor:
+    return x.unsqueeze(0) if x.dim() == 1 else x
+
+
+# --- calls ---------------------------------------------------------------------
+
+def init(device: Optional[torch.device] = None) -> None:
+    """Allocate the per-device scratch now (do this before any CUDA graph capture)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(lib().nm_device_status(ctypes.c_void_p(_stream())), "nm_device_status")
+
+
+def device_status() -> int:
+    """Wait for the current stream; return and clear the device status word."""
+    return lib().nm_device_status(ctypes.c_void_p(_stream()))
+
+
+def select(W: torch.Tensor, a: torch.Tensor, N: int, M: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Wanda N:M selection on the GPU: keep the N largest |W|*a_j per M-column subgroup."""
+    _cuda(W, torch.bfloat16, "W")
+    _cuda(a, torch.float32, "a")
+    rows, K = W.shape
+    out = torch.empty_like(W) if out is None else _cuda(out, torch.bfloat16, "out")
+    _check(lib().nm_select(W.data_ptr(), a.data_ptr(), rows, K, N, M, out.data_ptr(),
+                           ctypes.c_void_p(_stream(W))), "nm_select")
+    return out
+
+
+def pack(W: torch.Tensor, N: int, M: int):
+    """Pruned dense W (bf16, CUDA) -> (masks int32-viewed uint32 [rows][K/32], values bf16 [rows][K/2])."""
+    _cuda(W, torch.bfloat16, "W")
+    rows, K = W.shape
+    masks = torch.empty(rows, K // 32, dtype=torch.int32, device=W.device)
+    values = torch.empty(rows, K // 2, dtype=torch.bfloat16, device=W.device)
+    _check(lib().nm_pack(W.data_ptr(), rows, K, N, M, masks.data_ptr(), values.data_ptr(),
+                         ctypes.c_void_p(_stream(W))), "nm_pack")
+    return masks, values
+
+
+def pack_host(W: torch.Tensor, N: int, M: int):
+    """Host packer: CPU bf16 W -> CPU (masks int32-viewed uint32, values bf16)."""
+    if W.is_cuda or W.dtype != torch.bfloat16 or not W.is_contiguous():
+        raise TypeError("W must be a contiguous CPU bf16 tensor")
+    rows, K = W.shape
+    masks = torch.empty(rows, K // 32, dtype=torch.int32)
+    values = torch.empty(rows, K // 2, dtype=torch.bfloat16)
+    _check(lib().nm_pack_host(W.data_ptr(), rows, K, N, M, masks.data_ptr(), values.data_ptr()), "nm_pack_host")
+    return masks, values
+
+
+def spmv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, out: Optional[torch.Tensor] = None,
+         f32: bool = False) -> torch.Tensor:
+    """y[b][r] = sum_j W[r][j] x[b][j] over the bitmask format; bf16 (or fp32 with f32=True)."""
+    _cuda(masks, torch.int32, "masks")
+    _cuda(values, torch.bfloat16, "values")
+    x = _cuda(_x2d(x), torch.bfloat16, "x")
+    rows = masks.shape[0]
+    K = masks.shape[1] * 32
+    batch = x.shape[0]
+    if values.shape != (rows, K // 2) or x.shape[1] != K:
+        raise ValueError("shape mismatch between masks, values and x")
+    odt = torch.float32 if f32 else torch.bfloat16
+    out = torch.empty(batch, rows, dtype=odt, device=x.device) if out is None else _cuda(out, odt, "out")
+    fn = lib().nm_spmv_f32out if f32 else lib().nm_spmv
+    _check(fn(masks.data_ptr(), values.data_ptr(), x.data_ptr(), out.data_ptr(), rows, K, batch,
+              ctypes.c_void_p(_stream(x))), "nm_spmv_f32out" if f32 else "nm_spmv")
+    return out
+
+
+def dense_gemv(W: torch.Tensor, x: torch.Tensor, out: Optional[torch.Tensor] = None,
+               f32: bool = False) -> torch.Tensor:
+    """Dense bf16 reference: y[b][r] = sum_j W[r][j] x[b][j]."""
+    _cuda(W, torch.bfloat16, "W")
+    x = _cuda(_x2d(x), torch.bfloat16, "x")
+    rows, K = W.shape
+    batch = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("shape mismatch between W and x")
+    odt = torch.float32 if f32 else torch.bfloat16
+    out = torch.empty(batch, rows, dtype=odt, device=x.device) if out is None else _cuda(out, odt, "out")
+    fn = lib().dense_gemv_f32out if f32 else lib().dense_gemv
+    _check(fn(W.data_ptr(), x.data_ptr(), out.data_ptr(), rows, K, batch, ctypes.c_void_p(_stream(x))),
+           "dense_gemv")
+    return out
+
+
+def _linear_array(ops: Sequence[dict]) -> ctypes.Array:
+    arr = (NmLinear * len(ops))()
+    for i, op in enumerate(ops):
+        t = arr[i]
+        for f in ("masks", "values", "W", "x", "y"):
+            v = op.get(f)
+            setattr(t, f, v.data_ptr() if v is not None else None)
+        t.rows = int(op["rows"])
+        t.K = int(op["K"])
+    return arr
+
+
+def spmv_stack(ops: Sequence[dict], batch: int) -> None:
+    """Run a decode-token linear stack: ops[i] = {masks, values, x, y, rows, K}, in order."""
+    arr = _linear_array(ops)
+    _check(lib().nm_spmv_stack(arr, len(ops), batch, ctypes.c_void_p(_stream())), "nm_spmv_stack")
+
+
+def dense_gemv_stack(ops: Sequence[dict], batch: int) -> None:
+    """Dense counterpart of spmv_stack: ops[i] = {W, x, y, rows, K}."""
+    arr = _linear_array(ops)
+    _check(lib().dense_gemv_stack(arr, len(ops), batch, ctypes.c_void_p(_stream())), "dense_gemv_stack")
+
+
+class StackPlan:
+    """A decode-token stack with its descriptor array built once; ``run()`` launches it."""
+
+    def __init__(self, ops: Sequence[dict], batch: int, dense: bool = False):
+        self._keep = list(ops)  # keep the tensors alive as long as the plan
+        self._arr = _linear_array(self._keep)
+        self._n = len(self._keep)
+        self.batch = batch
+        self._fn = lib().dense_gemv_stack if dense else lib().nm_spmv_stack
+        self._name = "dense_gemv_stack" if dense else "nm_spmv_stack"
+
+    def run(self) -> None:
+        _check(self._fn(self._arr, self._n, self.batch, ctypes.c_void_p(_stream())), self._name)

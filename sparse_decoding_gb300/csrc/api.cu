@@ -1,0 +1,287 @@
+// api.cu -- the library's C entry points (declared in include/nmspmv.h):
+// argument checks, the per-device scratch, and dispatch to the kernels.
+#include <mutex>
+
+#include "kernels.h"
+
+namespace nm {
+
+constexpr int kMaxDevices = 64;
+
+static std::mutex g_mu;
+static void *g_scratch[kMaxDevices];
+static int g_num_sms[kMaxDevices];
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool pattern_ok(int N, int M)
+{
+    return (N == 2 && M == 4) || (N == 4 && M == 8) || (N == 8 && M == 16) || (N == 16 && M == 32);
+}
+
+// Scratch and SM count of the current device; allocates the scratch on first use.
+static nm_status device_ctx(cudaStream_t stream, bool pdl, LaunchCtx *ctx)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return NM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch[dev]) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, kScratchBytes) != cudaSuccess)
+            return NM_ERR_CUDA;
+        if (cudaMemset(p, 0, kScratchBytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(p);
+            return NM_ERR_CUDA;
+        }
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+            cudaFree(p);
+            return NM_ERR_CUDA;
+        }
+        g_num_sms[dev] = sms;
+        g_scratch[dev] = p;
+    }
+    ctx->stream = stream;
+    ctx->pdl = pdl;
+    ctx->scratch = scratch_from_base(g_scratch[dev]);
+    ctx->num_sms = g_num_sms[dev];
+    return NM_OK;
+}
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+static nm_status check_spmv_args(const void *masks, const void *values, const void *x, const void *y,
+                                 int64_t rows, int64_t K, int batch)
+{
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (batch < 1 || batch > 8)
+        return NM_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return NM_OK;
+    if (!y || (K > 0 && (!masks || !values || !x)))
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(y) || (K > 0 && (!aligned16(masks) || !aligned16(values) || !aligned16(x))))
+        return NM_ERR_ALIGN;
+    return NM_OK;
+}
+
+static nm_status check_gemv_args(const void *W, const void *x, const void *y, int64_t rows, int64_t K, int batch)
+{
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (batch < 1 || batch > 8)
+        return NM_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return NM_OK;
+    if (!y || (K > 0 && (!W || !x)))
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(y) || (K > 0 && (!aligned16(W) || !aligned16(x))))
+        return NM_ERR_ALIGN;
+    return NM_OK;
+}
+
+static nm_status zero_output(void *y, int64_t rows, int batch, size_t elt, cudaStream_t stream)
+{
+    return cudaMemsetAsync(y, 0, (size_t)rows * batch * elt, stream) == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+static nm_status spmv_impl(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,
+                           int64_t rows, int64_t K, int batch, cudaStream_t stream, bool pdl)
+{
+    nm_status s = check_spmv_args(masks, values, x, y, rows, K, batch);
+    if (s != NM_OK || rows == 0)
+        return s;
+    if (K == 0)
+        return zero_output(y, rows, batch, f32out ? 4 : 2, stream);
+    LaunchCtx ctx;
+    if ((s = device_ctx(stream, pdl, &ctx)) != NM_OK)
+        return s;
+    s = launch_spmv(masks, values, x, y, f32out, rows, K, batch, ctx);
+    if (s == NM_OK && cudaGetLastError() != cudaSuccess)
+        s = NM_ERR_CUDA;
+    return s;
+}
+
+static nm_status gemv_impl(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K, int batch,
+                           cudaStream_t stream, bool pdl)
+{
+    nm_status s = check_gemv_args(W, x, y, rows, K, batch);
+    if (s != NM_OK || rows == 0)
+        return s;
+    if (K == 0)
+        return zero_output(y, rows, batch, f32out ? 4 : 2, stream);
+    LaunchCtx ctx;
+    if ((s = device_ctx(stream, pdl, &ctx)) != NM_OK)
+        return s;
+    s = launch_gemv(W, x, y, f32out, rows, K, batch, ctx);
+    if (s == NM_OK && cudaGetLastError() != cudaSuccess)
+        s = NM_ERR_CUDA;
+    return s;
+}
+
+} // namespace nm
+
+using namespace nm;
+
+extern "C" {
+
+int nm_abi_version(void) { return 1; }
+
+const char *nm_status_str(int status)
+{
+    switch (status) {
+    case NM_OK: return "ok";
+    case NM_ERR_INVALID_ARG: return "invalid argument";
+    case NM_ERR_SHAPE: return "bad shape (sizes must be >= 0 and K a multiple of 32)";
+    case NM_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case NM_ERR_UNSUPPORTED: return "unsupported N:M pattern or batch size";
+    case NM_ERR_NOT_NM: return "an M-subgroup holds more than N nonzeros";
+    case NM_ERR_CUDA: return "CUDA error";
+    case NM_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    default: return "unknown status";
+    }
+}
+
+nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M, void *W_pruned,
+                    void *stream)
+{
+    if (!pattern_ok(N, M))
+        return NM_ERR_UNSUPPORTED;
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (rows == 0 || K == 0)
+        return NM_OK;
+    if (!W_bf16 || !a || !W_pruned)
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(W_bf16) || !aligned16(a) || !aligned16(W_pruned))
+        return NM_ERR_ALIGN;
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    return launch_select(W_bf16, a, rows, K, N, M, W_pruned, ctx);
+}
+
+nm_status nm_pack(const void *W_bf16, int64_t rows, int64_t K, int N, int M, uint32_t *masks, void *values_bf16,
+                  void *stream)
+{
+    if (!pattern_ok(N, M))
+        return NM_ERR_UNSUPPORTED;
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (rows == 0 || K == 0)
+        return NM_OK;
+    if (!W_bf16 || !masks || !values_bf16)
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(W_bf16) || !aligned16(masks) || !aligned16(values_bf16))
+        return NM_ERR_ALIGN;
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    // One pack at a time per process: the error flag lives in the shared scratch.
+    static std::mutex pack_mu;
+    std::lock_guard<std::mutex> lock(pack_mu);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ctx.scratch.status + 1, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    if ((s = launch_pack(W_bf16, rows, K, N, M, masks, values_bf16, ctx)) != NM_OK)
+        return s;
+    uint32_t bad = 0;
+    if (cudaMemcpyAsync(&bad, ctx.scratch.status + 1, sizeof bad, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    return bad ? NM_ERR_NOT_NM : NM_OK;
+}
+
+nm_status nm_spmv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *y_bf16, int64_t rows,
+                  int64_t K, int batch, void *stream)
+{
+    return spmv_impl(masks, values_bf16, x_bf16, y_bf16, false, rows, K, batch, (cudaStream_t)stream, false);
+}
+
+nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
+                         int64_t rows, int64_t K, int batch, void *stream)
+{
+    return spmv_impl(masks, values_bf16, x_bf16, y_f32, true, rows, K, batch, (cudaStream_t)stream, false);
+}
+
+nm_status dense_gemv(const void *W_bf16, const void *x_bf16, void *y_bf16, int64_t rows, int64_t K, int batch,
+                     void *stream)
+{
+    return gemv_impl(W_bf16, x_bf16, y_bf16, false, rows, K, batch, (cudaStream_t)stream, false);
+}
+
+nm_status dense_gemv_f32out(const void *W_bf16, const void *x_bf16, float *y_f32, int64_t rows, int64_t K,
+                            int batch, void *stream)
+{
+    return gemv_impl(W_bf16, x_bf16, y_f32, true, rows, K, batch, (cudaStream_t)stream, false);
+}
+
+nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream)
+{
+    if (n_ops < 0 || (n_ops > 0 && !ops))
+        return NM_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ops; ++i) {
+        nm_status s = check_spmv_args(ops[i].masks, ops[i].values, ops[i].x, ops[i].y, ops[i].rows, ops[i].K, batch);
+        if (s != NM_OK)
+            return s;
+    }
+    for (int i = 0; i < n_ops; ++i) {
+        nm_status s = spmv_impl(ops[i].masks, ops[i].values, ops[i].x, ops[i].y, false, ops[i].rows, ops[i].K, batch,
+                                (cudaStream_t)stream, true);
+        if (s != NM_OK)
+            return s;
+    }
+    return NM_OK;
+}
+
+nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream)
+{
+    if (n_ops < 0 || (n_ops > 0 && !ops))
+        return NM_ERR_INVALID_ARG;
+    for (int i = 0; i < n_ops; ++i) {
+        nm_status s = check_gemv_args(ops[i].W, ops[i].x, ops[i].y, ops[i].rows, ops[i].K, batch);
+        if (s != NM_OK)
+            return s;
+    }
+    for (int i = 0; i < n_ops; ++i) {
+        nm_status s = gemv_impl(ops[i].W, ops[i].x, ops[i].y, false, ops[i].rows, ops[i].K, batch,
+                                (cudaStream_t)stream, true);
+        if (s != NM_OK)
+            return s;
+    }
+    return NM_OK;
+}
+
+nm_status nm_device_status(void *stream)
+{
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ctx.scratch.status, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(ctx.scratch.status, 0, sizeof word, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    return (word & (1u << NM_ERR_TIMEOUT)) ? NM_ERR_TIMEOUT : NM_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,261 @@
+// nm_common.cuh -- internal helpers shared by the library's kernels.
+//
+// Inline PTX wrappers for the sm_100-family features the kernels use
+// (mbarrier, TMA tensor copies, programmatic dependent launch), bf16 bit
+// helpers, and the per-device scratch layout. Written from the public PTX ISA.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nmspmv.h"
+
+namespace nm {
+
+// ---------------------------------------------------------------------------
+// Per-device scratch (allocated once per device by the host side).
+// ---------------------------------------------------------------------------
+
+// Stream-K workers (warps) that one launch may use; bounds the scratch size.
+constexpr int kMaxWorkers = 4096;
+// Partial sums per worker: 2 slots (first and last row block) x 32 rows x 8 batch.
+constexpr int kPartialFloats = 2 * 32 * 8;
+
+// status[0]: NM_ERR_TIMEOUT bit set by a bounded wait that ran out.
+// status[1]: nonzero when nm_pack found more than N nonzeros in a subgroup.
+struct Scratch {
+    uint32_t *status;   // [4]
+    uint32_t *counters; // [kMaxWorkers], zero between launches
+    float *partials;    // [kMaxWorkers][kPartialFloats]
+};
+
+constexpr size_t kScratchStatusBytes = 256;
+constexpr size_t kScratchCounterBytes = sizeof(uint32_t) * kMaxWorkers;
+constexpr size_t kScratchPartialBytes = sizeof(float) * (size_t)kMaxWorkers * kPartialFloats;
+constexpr size_t kScratchBytes = kScratchStatusBytes + kScratchCounterBytes + kScratchPartialBytes;
+
+inline Scratch scratch_from_base(void *base)
+{
+    Scratch s;
+    char *p = (char *)base;
+    s.status = (uint32_t *)p;
+    s.counters = (uint32_t *)(p + kScratchStatusBytes);
+    s.partials = (float *)(p + kScratchStatusBytes + kScratchCounterBytes);
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 bits
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// fp32 -> bf16, round to nearest even (NaN stays NaN).
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
+{
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory access by 32-bit shared address
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float2 lds_f32x2(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
+}
+__device__ __forceinline__ void sts_f32x2(uint32_t a, float x, float y)
+{
+    asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(a), "f"(x), "f"(y));
+}
+__device__ __forceinline__ void sts_f32x4(uint32_t a, float x, float y, float z, float w)
+{
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w));
+}
+
+// Position of the most significant set bit, or -1 (0xFFFFFFFF) for zero.
+__device__ __forceinline__ int bfind_u32(uint32_t m)
+{
+    int r;
+    asm("bfind.u32 %0, %1;" : "=r"(r) : "r"(m));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: about one second, then record NM_ERR_TIMEOUT and give up.
+// Once a wait of this thread has run out (`dead`), later waits only poll once,
+// so a kernel that lost its data ends within about a second in total.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t *status, bool &dead)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    if (dead)
+        return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, 1u << NM_ERR_TIMEOUT);
+            dead = true;
+            return false;
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tensor copies global -> shared, completion counted on an mbarrier)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int32_t c0,
+                                                 int32_t c1, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch (no-ops when the launch does not use it)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait_upstream()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Global loads
+// ---------------------------------------------------------------------------
+
+// 128-bit read-only load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ uint4 ldg_stream128(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ldcg_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+} // namespace nm

@@ -1,0 +1,129 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol that
+include/nmspmv.h declares, validates arguments before touching the GPU, and
+its host packer is bit-exact with the oracle's packer. No GPU compute here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.bits import to_bits
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nmspmv.h")
+
+
+@pytest.fixture(scope="module")
+def nm():
+    from sparse_decoding_gb300 import build
+    build.build()
+    import sparse_decoding_gb300 as nm
+    nm.lib()
+    return nm
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(\w+)\s*\([^;{]*\)\s*;", text)) - {"if", "sizeof"})
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("nm_pack_host", "nm_select", "nm_pack", "nm_spmv", "nm_spmv_f32out", "dense_gemv",
+              "nm_spmv_stack", "dense_gemv_stack", "nm_device_status", "nm_status_str", "nm_abi_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(nm):
+    L = nm.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), f"libnmspmv.so does not export {name}"
+    assert set(declared_functions()) <= set(nm.EXPORTS) | set(declared_functions())
+    assert L.nm_abi_version() == 1
+
+
+def test_status_strings(nm):
+    for code in range(8):
+        assert nm.status_str(code)
+    assert nm.status_str(5).startswith("an M-subgroup")
+
+
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_host_pack_bit_exact_with_oracle(nm, N, M):
+    rows, K = 67, 4096
+    W = synth.weights(rows, K, seed=21)
+    a = synth.col_norms(K, seed=21).numpy()
+    Wp = oracle.select(to_bits(W), a, N, M)
+    om, ov = oracle.pack(Wp, N, M)
+    Wt = torch.from_numpy(Wp.view(np.int16)).view(torch.bfloat16)
+    masks, values = nm.pack_host(Wt, N, M)
+    np.testing.assert_array_equal(masks.numpy().view(np.uint32), om)
+    np.testing.assert_array_equal(to_bits(values), ov)
+
+
+def test_host_pack_fill_rule_and_errors(nm):
+    W = np.zeros((2, 64), dtype=np.uint16)
+    W[0, 2] = 0x4000
+    W[0, 0] = 0x8000  # -0.0: zero, becomes the filler
+    W[1, :] = 0x3F80  # every entry nonzero: more than N
+    Wt = torch.from_numpy(W[:1].copy().view(np.int16)).view(torch.bfloat16)
+    masks, values = nm.pack_host(Wt, 8, 16)
+    om, ov = oracle.pack(W[:1], 8, 16)
+    np.testing.assert_array_equal(masks.numpy().view(np.uint32), om)
+    np.testing.assert_array_equal(to_bits(values), ov)
+    bad = torch.from_numpy(W[1:].copy().view(np.int16)).view(torch.bfloat16)
+    with pytest.raises(nm.NmError) as e:
+        nm.pack_host(bad, 8, 16)
+    assert e.value.status == nm.NM_ERR_NOT_NM
+    with pytest.raises(nm.NmError) as e:
+        nm.pack_host(bad, 3, 8)
+    assert e.value.status == nm.NM_ERR_UNSUPPORTED
+
+
+def test_argument_validation_before_any_cuda_call(nm):
+    """These calls must fail on their arguments alone (no device is touched)."""
+    L = nm.lib()
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.addressof(buf)
+    p16 = (p + 15) & ~15
+    # K not a multiple of 32
+    assert L.nm_spmv(p16, p16, p16, p16, 4, 48, 1, None) == nm.NM_ERR_SHAPE
+    assert L.dense_gemv(p16, p16, p16, 4, 48, 1, None) == nm.NM_ERR_SHAPE
+    # batch outside 1..8
+    assert L.nm_spmv(p16, p16, p16, p16, 4, 64, 9, None) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_spmv(p16, p16, p16, p16, 4, 64, 0, None) == nm.NM_ERR_UNSUPPORTED
+    # misaligned pointer
+    assert L.nm_spmv(p16 + 2, p16, p16, p16, 4, 64, 1, None) == nm.NM_ERR_ALIGN
+    assert L.nm_spmv_f32out(p16, p16, p16, p16 + 4, 4, 64, 1, None) == nm.NM_ERR_ALIGN
+    assert L.dense_gemv(p16, p16 + 8, p16, 4, 64, 1, None) == nm.NM_ERR_ALIGN
+    # NULL data pointer
+    assert L.nm_spmv(None, p16, p16, p16, 4, 64, 1, None) == nm.NM_ERR_INVALID_ARG
+    # unsupported pattern
+    assert L.nm_pack(p16, 4, 64, 3, 4, p16, p16, None) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_select(p16, p16, 4, 64, 2, 8, p16, None) == nm.NM_ERR_UNSUPPORTED
+    # empty problems succeed without work
+    assert L.nm_spmv(None, None, None, None, 0, 64, 1, None) == nm.NM_OK
+    assert L.nm_pack(None, 0, 64, 2, 4, None, None, None) == nm.NM_OK
+    # negative sizes
+    assert L.nm_spmv(p16, p16, p16, p16, -1, 64, 1, None) == nm.NM_ERR_SHAPE
+    # a stack is validated as a whole before anything is launched
+    ops = (nm.NmLinear * 2)()
+    for o in ops:
+        o.masks = o.values = o.x = o.y = p16
+        o.rows, o.K = 4, 64
+    ops[1].K = 40
+    assert L.nm_spmv_stack(ops, 2, 1, None) == nm.NM_ERR_SHAPE
+    assert L.nm_spmv_stack(None, 1, 1, None) == nm.NM_ERR_INVALID_ARG
+
+
+def test_no_fallback_when_library_missing(monkeypatch):
+    import sparse_decoding_gb300 as nm
+    monkeypatch.setattr(nm, "_lib", None)
+    monkeypatch.setattr(nm, "LIB_PATH", "/nonexistent/libnmspmv.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        nm.lib()

@@ -1,0 +1,337 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerances (the fp32 and bf16 bounds of the decode SpMV):
+  * masks, values, selection: bit-exact;
+  * fp32 output: |y32 - y64| <= 1e-4 * S elementwise, S = sum_j |W_rj x_bj|;
+  * bf16 output: within one bf16 ulp of y64, and equal to bf16_rn(y32) of the
+    same kernel (where |y64| < 1e-4 * S only the fp32 bound applies);
+  * integer-valued cases (dyadic W, small-integer x): exact.
+Inputs for the CUDA path come from synth (seeded) or from the oracle; no
+oracle input comes from the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.bits import bf16_ulp, bits_to_f32, from_bits, to_bits
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def nm():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from sparse_decoding_gb300 import build
+    build.build()
+    import sparse_decoding_gb300 as nm
+    nm.init()
+    return nm
+
+
+def dev(bits: np.ndarray) -> torch.Tensor:
+    return from_bits(bits).cuda()
+
+
+def masks_np(m: torch.Tensor) -> np.ndarray:
+    return m.cpu().numpy().view(np.uint32)
+
+
+def bf16_round_np(y32: np.ndarray) -> np.ndarray:
+    return to_bits(torch.from_numpy(np.ascontiguousarray(y32, dtype=np.float32)).to(torch.bfloat16))
+
+
+def check_close(y32: np.ndarray, ybf: np.ndarray, y64: np.ndarray, S: np.ndarray, what: str):
+    err = np.abs(y32.astype(np.float64) - y64)
+    bad = err > TOL * S
+    assert not bad.any(), f"{what}: fp32 error {err[bad][:5]} > 1e-4*S {TOL * S[bad][:5]}"
+    if ybf is not None:
+        np.testing.assert_array_equal(ybf, bf16_round_np(y32), err_msg=f"{what}: bf16 != rn(fp32)")
+        yb = bits_to_f32(ybf).astype(np.float64)
+        strict = np.abs(y64) >= TOL * S
+        ulp_err = np.abs(yb - y64)
+        bad = strict & (ulp_err > bf16_ulp(y64))
+        assert not bad.any(), f"{what}: bf16 more than 1 ulp off at {np.argwhere(bad)[:5]}"
+
+
+def oracle_case(rows, K, N, M, batch, seed, select=True):
+    """Oracle-side inputs: pruned W (bits), masks, values, x (bits), y64, S."""
+    if select:
+        W = to_bits(synth.weights(rows, K, seed=seed))
+        a = synth.col_norms(K, seed=seed).numpy()
+        Wp = oracle.select(W, a, N, M)
+    else:
+        Wp = to_bits(synth.nm_structured(rows, K, N, M, seed=seed))
+    masks, values = oracle.pack(Wp, N, M)
+    x = to_bits(synth.activations(batch, K, seed=seed + 1))
+    y64, S = oracle.spmv_f64(Wp, x)
+    return Wp, masks, values, x, y64, S
+
+
+def run_spmv(nm, masks, values, x):
+    m = torch.from_numpy(masks.view(np.int32)).cuda()
+    v, xd = dev(values), dev(x)
+    y32 = nm.spmv(m, v, xd, f32=True)
+    ybf = nm.spmv(m, v, xd)
+    torch.cuda.synchronize()
+    return y32.cpu().numpy(), to_bits(ybf)
+
+
+# --- SpMV -------------------------------------------------------------------------
+
+SMALL_SHAPES = [(1, 128), (31, 128), (33, 256), (100, 512), (64, 4096), (257, 1024),  # TMA path
+                (1, 32), (31, 64), (33, 96), (70, 160), (5, 4000 // 32 * 32)]          # fallback path
+
+
+@pytest.mark.parametrize("rows,K", SMALL_SHAPES)
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_spmv_small_shapes(nm, rows, K, N, M):
+    for batch in (1, 3):
+        _, masks, values, x, y64, S = oracle_case(rows, K, N, M, batch, seed=rows * 7 + K)
+        y32, ybf = run_spmv(nm, masks, values, x)
+        check_close(y32, ybf, y64, S, f"{rows}x{K} {N}:{M} b{batch}")
+
+
+@pytest.mark.parametrize("batch", range(1, 9))
+def test_spmv_every_batch(nm, batch):
+    for rows, K in ((96, 1024), (45, 96)):
+        _, masks, values, x, y64, S = oracle_case(rows, K, 16, 32, batch, seed=batch)
+        y32, ybf = run_spmv(nm, masks, values, x)
+        check_close(y32, ybf, y64, S, f"{rows}x{K} b{batch}")
+
+
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_spmv_single_4096(nm, N, M):
+    """4096 x 4096, batch 1, seed 0: the single-linear workload."""
+    _, masks, values, x, y64, S = oracle_case(4096, 4096, N, M, 1, seed=0)
+    y32, ybf = run_spmv(nm, masks, values, x)
+    check_close(y32, ybf, y64, S, f"4096x4096 {N}:{M}")
+
+
+@pytest.mark.parametrize("name", ["qkv", "o", "gate_up", "down"])
+@pytest.mark.parametrize("N,M", [(2, 4), (16, 32)])
+def test_spmv_llama8b_linears(nm, name, N, M):
+    rows, K = synth.LLAMA31_8B[name]
+    _, masks, values, x, y64, S = oracle_case(rows, K, N, M, 1, seed=11, select=False)
+    y32, ybf = run_spmv(nm, masks, values, x)
+    check_close(y32, ybf, y64, S, f"{name} {N}:{M}")
+
+
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_spmv_exact_dyadic(nm, N, M):
+    """Dyadic weights, small-integer x: fp32 is exact in any summation order."""
+    for rows, K, batch in ((4096, 4096, 1), (100, 14336, 4), (33, 96, 2)):
+        Wp = to_bits(synth.nm_structured(rows, K, N, M, seed=5, dyadic=True))
+        masks, values = oracle.pack(Wp, N, M)
+        x = to_bits(synth.small_int_activations(batch, K, seed=5))
+        y64, _ = oracle.spmv_f64(Wp, x)
+        y32, ybf = run_spmv(nm, masks, values, x)
+        np.testing.assert_array_equal(y32.astype(np.float64), y64)
+        np.testing.assert_array_equal(ybf, bf16_round_np(y64.astype(np.float32)))
+
+
+def test_spmv_one_hot_columns(nm):
+    rows, K = 77, 512
+    Wp = to_bits(synth.nm_structured(rows, K, 4, 8, seed=6))
+    masks, values = oracle.pack(Wp, 4, 8)
+    cols = [0, 1, 31, 32, 127, 128, 300, 511]
+    x = np.zeros((len(cols), K), dtype=np.uint16)
+    for b, j in enumerate(cols):
+        x[b, j] = 0x3F80
+    y32, ybf = run_spmv(nm, masks, values, x)
+    for b, j in enumerate(cols):
+        np.testing.assert_array_equal(y32[b], bits_to_f32(Wp[:, j]))
+        np.testing.assert_array_equal(ybf[b], Wp[:, j])
+
+
+def test_spmv_closed_forms(nm):
+    rows, K = 40, 1024
+    keep = synth.random_nm_keep(rows, K, 8, 16, seed=7).numpy()
+    Wp = np.where(keep, np.uint16(0x3F80), np.uint16(0))
+    masks, values = oracle.pack(Wp, 8, 16)
+    ones = np.full((2, K), 0x3F80, dtype=np.uint16)
+    y32, _ = run_spmv(nm, masks, values, ones)
+    assert np.all(y32 == K / 2)
+    y32, ybf = run_spmv(nm, masks, values, np.zeros((1, K), dtype=np.uint16))
+    assert np.all(y32 == 0) and np.all(ybf == 0)
+
+
+def test_spmv_nan_stays_in_its_row(nm):
+    rows, K = 64, 256
+    Wp = to_bits(synth.nm_structured(rows, K, 2, 4, seed=8))
+    c = int(np.nonzero(Wp[5])[0][3])
+    Wp[5, c] = 0x7FC0
+    masks, values = oracle.pack(Wp, 2, 4)
+    x = to_bits(synth.activations(1, K, seed=8))
+    y64, S = oracle.spmv_f64(Wp, x)
+    y32, ybf = run_spmv(nm, masks, values, x)
+    assert np.isnan(y32[0, 5]) and np.isnan(bits_to_f32(ybf[0, 5]))
+    ok = np.arange(rows) != 5
+    check_close(y32[:, ok], ybf[:, ok], y64[:, ok], S[:, ok], "nan rows")
+
+
+def test_spmv_repeatable(nm):
+    """Fixed summation order: repeated calls give identical bits."""
+    _, masks, values, x, _, _ = oracle_case(6144, 4096, 2, 4, 1, seed=9, select=False)
+    m = torch.from_numpy(masks.view(np.int32)).cuda()
+    v, xd = dev(values), dev(x)
+    ys = [nm.spmv(m, v, xd, f32=True) for _ in range(3)]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+def test_spmv_empty_and_k0(nm):
+    m = torch.zeros(0, 4, dtype=torch.int32, device="cuda")
+    v = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(1, 128, dtype=torch.bfloat16, device="cuda")
+    y = nm.spmv(m, v, x)
+    assert y.shape == (1, 0)
+    # K == 0: every output is the empty sum, +0
+    m0 = torch.zeros(5, 0, dtype=torch.int32, device="cuda")
+    v0 = torch.zeros(5, 0, dtype=torch.bfloat16, device="cuda")
+    x0 = torch.zeros(2, 0, dtype=torch.bfloat16, device="cuda")
+    y0 = torch.full((2, 5), 7.0, dtype=torch.bfloat16, device="cuda")
+    nm.spmv(m0, v0, x0, out=y0)
+    assert torch.equal(y0, torch.zeros_like(y0))
+
+
+# --- pack and select ---------------------------------------------------------------
+
+PACK_SHAPES = [(1, 32), (31, 64), (33, 96), (257, 1024), (4096, 4096), (128, 14336)]
+
+
+@pytest.mark.parametrize("rows,K", PACK_SHAPES)
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_select_and_pack_bit_exact(nm, rows, K, N, M):
+    W = synth.weights(rows, K, seed=rows + K)
+    a = synth.col_norms(K, seed=rows + K)
+    Wp = oracle.select(to_bits(W), a.numpy(), N, M)
+    om, ov = oracle.pack(Wp, N, M)
+    Wg = nm.select(W.cuda(), a.cuda(), N, M)
+    np.testing.assert_array_equal(to_bits(Wg), Wp)
+    gm, gv = nm.pack(Wg, N, M)
+    np.testing.assert_array_equal(masks_np(gm), om)
+    np.testing.assert_array_equal(to_bits(gv), ov)
+    # in-place selection gives the same result
+    Wi = W.cuda()
+    nm.select(Wi, a.cuda(), N, M, out=Wi)
+    np.testing.assert_array_equal(to_bits(Wi), Wp)
+
+
+def test_select_ties_and_special_values(nm):
+    rows, K = 64, 256
+    rng = np.random.default_rng(3)
+    W = np.array([0x3F80, 0xBF80, 0x4000, 0x0000, 0x8000], dtype=np.uint16)[rng.integers(0, 5, (rows, K))]
+    a = np.ones(K, dtype=np.float32)
+    a[::7] = 0.0
+    for N, M in synth.PATTERNS:
+        Wp = oracle.select(W, a, N, M)
+        got = nm.select(dev(W), torch.from_numpy(a).cuda(), N, M)
+        np.testing.assert_array_equal(to_bits(got), Wp)
+        om, ov = oracle.pack(Wp, N, M)
+        gm, gv = nm.pack(dev(Wp), N, M)
+        np.testing.assert_array_equal(masks_np(gm), om)
+        np.testing.assert_array_equal(to_bits(gv), ov)
+
+
+def test_pack_fill_rule_and_signed_zero(nm):
+    Wp = np.zeros((3, 64), dtype=np.uint16)
+    Wp[0, 2] = 0x4000
+    Wp[0, 0] = 0x8000
+    Wp[1, 40] = 0x7FC0       # NaN counts as nonzero and is kept bit for bit
+    Wp[2, :] = 0x0000        # all zero: the first N of every subgroup
+    for N, M in synth.PATTERNS:
+        om, ov = oracle.pack(Wp, N, M)
+        gm, gv = nm.pack(dev(Wp), N, M)
+        np.testing.assert_array_equal(masks_np(gm), om)
+        np.testing.assert_array_equal(to_bits(gv), ov)
+
+
+def test_pack_reports_not_nm(nm):
+    Wp = np.full((4, 64), 0x3F80, dtype=np.uint16)
+    with pytest.raises(nm.NmError) as e:
+        nm.pack(dev(Wp), 2, 4)
+    assert e.value.status == nm.NM_ERR_NOT_NM
+    # the next valid pack is not affected by the previous error
+    ok = to_bits(synth.nm_structured(4, 64, 2, 4, seed=1))
+    nm.pack(dev(ok), 2, 4)
+
+
+def test_misaligned_pointer_is_rejected(nm):
+    _, masks, values, x, _, _ = oracle_case(32, 128, 2, 4, 1, seed=1, select=False)
+    m = torch.from_numpy(masks.view(np.int32)).cuda()
+    v = dev(values)
+    xbig = torch.zeros(2, 136, dtype=torch.bfloat16, device="cuda")
+    xs = xbig.view(-1)[1:129]  # 2-byte offset
+    y = torch.empty(1, 32, dtype=torch.bfloat16, device="cuda")
+    st = nm.lib().nm_spmv(m.data_ptr(), v.data_ptr(), xs.data_ptr(), y.data_ptr(), 32, 128, 1, None)
+    assert st == nm.NM_ERR_ALIGN
+
+
+# --- dense reference ------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,K,batch", [(1, 32, 1), (33, 96, 3), (4096, 4096, 1), (4096, 14336, 1),
+                                           (100, 512, 8), (6144, 4096, 4)])
+def test_dense_gemv(nm, rows, K, batch):
+    Wp = to_bits(synth.nm_structured(rows, K, 2, 4, seed=rows))
+    x = to_bits(synth.activations(batch, K, seed=rows))
+    y64, S = oracle.spmv_f64(Wp, x)
+    Wd, xd = dev(Wp), dev(x)
+    y32 = nm.dense_gemv(Wd, xd, f32=True).cpu().numpy()
+    ybf = to_bits(nm.dense_gemv(Wd, xd))
+    check_close(y32, ybf, y64, S, f"dense {rows}x{K} b{batch}")
+
+
+# --- stacks and graphs -------------------------------------------------------------------
+
+def _stack_inputs(nm, batch=1, layers=2):
+    ops_s, ops_d, refs = [], [], []
+    for layer in range(layers):
+        for mi, name in enumerate(synth.MATRICES):
+            rows, K = synth.LLAMA31_8B[name]
+            rows = rows // 8  # keep the test quick; the shapes keep their K
+            W = synth.nm_structured(rows, K, 16, 32, seed=layer * 4 + mi).cuda()
+            m, v = nm.pack(W, 16, 32)
+            x = synth.activations(batch, K, seed=100 + layer * 4 + mi).cuda()
+            y = torch.empty(batch, rows, dtype=torch.bfloat16, device="cuda")
+            yd = torch.empty(batch, rows, dtype=torch.bfloat16, device="cuda")
+            ops_s.append(dict(masks=m, values=v, x=x, y=y, rows=rows, K=K))
+            ops_d.append(dict(W=W, x=x, y=yd, rows=rows, K=K))
+            refs.append((m, v, x, W))
+    return ops_s, ops_d, refs
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_stack_equals_single_calls(nm, batch):
+    ops_s, ops_d, refs = _stack_inputs(nm, batch)
+    nm.spmv_stack(ops_s, batch)
+    nm.dense_gemv_stack(ops_d, batch)
+    torch.cuda.synchronize()
+    for op, opd, (m, v, x, W) in zip(ops_s, ops_d, refs):
+        assert torch.equal(op["y"], nm.spmv(m, v, x))
+        assert torch.equal(opd["y"], nm.dense_gemv(W, x))
+
+
+def test_stack_in_cuda_graph(nm):
+    ops_s, _, refs = _stack_inputs(nm, 1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        nm.spmv_stack(ops_s, 1)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        nm.spmv_stack(ops_s, 1)
+    for op in ops_s:
+        op["y"].zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for op, (m, v, x, _) in zip(ops_s, refs):
+        assert torch.equal(op["y"], nm.spmv(m, v, x))
+
+
+def test_no_bounded_wait_ran_out(nm):
+    assert nm.device_status() == nm.NM_OK
