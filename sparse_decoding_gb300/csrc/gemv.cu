@@ -1,14 +1,19 @@
 // gemv.cu -- dense bf16 GEMV, the same-GPU dense reference for the sparse path
 // (the pages' 1.00x rows: aitest123.com article, Table 3).
 //
-// y[b][r] = sum_j W[r][j] x[b][j], fp32 accumulation. One warp per row: lane l
-// streams 16-byte chunks l, l+32, ... of the row with L1-bypassing loads (8
-// chunks in flight per lane), x comes through the read-only cache, and a
-// butterfly shuffle sums the 32 lane partials. Each CTA owns a contiguous
-// range of rows, so all SMs get the same number of weight bytes.
-#include <algorithm>
+// y[b][r] = sum_j W[r][j] x[b][j], fp32 accumulation.
+//
+// Main kernel (K % 64 == 0): the same stream-K TMA driver as the sparse
+// kernel (streamk.cuh), with units of 32 rows x 64 columns (4 KB of W, the
+// same bytes per unit as the sparse kernel's values). Lane i owns row i of the
+// unit; all lanes read the same x columns, so the x loads are broadcasts. The
+// two kernels differ only in the unit arithmetic, so their ratio measures the
+// format, not two different pipelines.
+//
+// Fallback kernel (K % 64 == 32): one warp per row with streaming loads.
+#include <string.h>
 
-#include "kernels.h"
+#include "streamk.cuh"
 
 namespace nm {
 
@@ -84,6 +89,94 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     pdl_launch_dependents();
 }
 
+constexpr int kDnCols = 64; // columns per unit
+
+// The dense unit: a 32 x 64 tile of W (128-byte swizzle) and the x slice.
+struct DenseUnit {
+    static constexpr int kCols = kDnCols;
+    static constexpr bool kHasMasks = false;
+    static constexpr int kWBytes = kUnitRows * kCols * 2;
+    static constexpr int kXOffset = kWBytes;
+    template <int B> static constexpr int stage_bytes() { return (kXOffset + 2 * kCols * B + 1023) / 1024 * 1024; }
+    template <int B> static constexpr uint32_t tx_bytes() { return kXOffset + 2 * kCols * B; }
+    template <int B> static constexpr int xf_bytes() { return kCols * BatchPad<B>::value * 4; }
+
+    static __device__ __forceinline__ void issue_weights(uint32_t st, uint32_t bar, int kc, int32_t row0,
+                                                         uint64_t pol, const TensorMaps &maps)
+    {
+        tma_load_2d_hint(st, &maps.w, kc * kCols, row0, bar, pol);
+    }
+
+    static constexpr int kSharedBytes = 0;
+    struct State {};
+    static __device__ __forceinline__ State initial_state() { return State{}; }
+    static __device__ __forceinline__ void init_shared(uint8_t *, int, int) {}
+
+    template <int B>
+    static __device__ __forceinline__ void consume(const uint8_t *stp, uint8_t *xf, const uint8_t *, State &, int lane,
+                                                   float (&acc)[4][B])
+    {
+        constexpr int BP = BatchPad<B>::value;
+        convert_x<B, kCols>(stp + kXOffset, xf, lane);
+        __syncwarp();
+        const uint8_t *roww = stp + lane * 128;
+        const int sw = lane & 7; // 16-byte chunk c of row r sits at c ^ (r & 7)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 t = *(const uint4 *)(roww + ((c ^ sw) << 4));
+            const uint32_t wp[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float w = (e & 1) ? bf16hi_to_f32(wp[e >> 1]) : bf16lo_to_f32(wp[e >> 1]);
+                const float *xa = (const float *)(xf + (8 * c + e) * BP * 4);
+                float xs[BP];
+                if (BP == 1) {
+                    xs[0] = xa[0];
+                } else if (BP == 2) {
+                    const float2 v = *(const float2 *)xa;
+                    xs[0] = v.x;
+                    xs[1 % BP] = v.y;
+                } else {
+#pragma unroll
+                    for (int b0 = 0; b0 < BP; b0 += 4) {
+                        const float4 v = *(const float4 *)(xa + b0);
+                        xs[b0 % BP] = v.x;
+                        xs[(b0 + 1) % BP] = v.y;
+                        xs[(b0 + 2) % BP] = v.z;
+                        xs[(b0 + 3) % BP] = v.w;
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+                    acc[c & 3][b] = fmaf(w, xs[b % BP], acc[c & 3][b]);
+            }
+        }
+    }
+};
+
+template <int B> struct DenseCfg {
+    static constexpr int W = B <= 2 ? 8 : B <= 4 ? 6 : 4;
+    static constexpr int NBUF = 2;
+    static constexpr int MINB = 2;
+};
+
+template <int B, bool F32OUT>
+static nm_status launch_gemv_tma(const void *W, const void *x, void *y, int64_t rows, int64_t K,
+                                 const LaunchCtx &ctx)
+{
+    TensorMaps maps;
+    memset(&maps.m, 0, sizeof maps.m);
+    nm_status s;
+    if ((s = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2,
+                       kDnCols, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
+        return s;
+    if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
+                       kDnCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+        return s;
+    return launch_streamk<DenseUnit, B, DenseCfg<B>::W, DenseCfg<B>::NBUF, DenseCfg<B>::MINB, F32OUT>(
+        maps, y, rows, K / kDnCols, ctx);
+}
+
 template <int B, bool F32OUT>
 static nm_status launch_gemv_b(const void *W, const void *x, void *y, int64_t rows, int64_t K,
                                const LaunchCtx &ctx)
@@ -110,17 +203,23 @@ template <bool F32OUT>
 static nm_status gemv_dispatch(const void *W, const void *x, void *y, int64_t rows, int64_t K, int batch,
                                const LaunchCtx &ctx)
 {
+    const bool tma = K % kDnCols == 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF;
+#define NM_CASE(BB)                                                                                         \
+    case BB:                                                                                                \
+        return tma ? launch_gemv_tma<BB, F32OUT>(W, x, y, rows, K, ctx) : launch_gemv_b<BB, F32OUT>(W, x, y, rows, K, ctx);
     switch (batch) {
-    case 1: return launch_gemv_b<1, F32OUT>(W, x, y, rows, K, ctx);
-    case 2: return launch_gemv_b<2, F32OUT>(W, x, y, rows, K, ctx);
-    case 3: return launch_gemv_b<3, F32OUT>(W, x, y, rows, K, ctx);
-    case 4: return launch_gemv_b<4, F32OUT>(W, x, y, rows, K, ctx);
-    case 5: return launch_gemv_b<5, F32OUT>(W, x, y, rows, K, ctx);
-    case 6: return launch_gemv_b<6, F32OUT>(W, x, y, rows, K, ctx);
-    case 7: return launch_gemv_b<7, F32OUT>(W, x, y, rows, K, ctx);
-    case 8: return launch_gemv_b<8, F32OUT>(W, x, y, rows, K, ctx);
-    default: return NM_ERR_UNSUPPORTED;
+        NM_CASE(1)
+        NM_CASE(2)
+        NM_CASE(3)
+        NM_CASE(4)
+        NM_CASE(5)
+        NM_CASE(6)
+        NM_CASE(7)
+        NM_CASE(8)
+    default:
+        return NM_ERR_UNSUPPORTED;
     }
+#undef NM_CASE
 }
 
 nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K, int batch,

@@ -17,22 +17,22 @@ namespace nm {
 // Per-device scratch (allocated once per device by the host side).
 // ---------------------------------------------------------------------------
 
-// Stream-K workers (warps) that one launch may use; bounds the scratch size.
-constexpr int kMaxWorkers = 4096;
-// Partial sums per worker: 2 slots (first and last row block) x 32 rows x 8 batch.
-constexpr int kPartialFloats = 2 * 32 * 8;
+// Stream-K CTAs that one launch may use; bounds the scratch size.
+constexpr int kMaxCtas = 1024;
+// Partial sums per CTA: 2 slots (first and last row block) x 8 batch x 32 rows.
+constexpr int kPartialFloats = 2 * 8 * 32;
 
 // status[0]: NM_ERR_TIMEOUT bit set by a bounded wait that ran out.
 // status[1]: nonzero when nm_pack found more than N nonzeros in a subgroup.
 struct Scratch {
     uint32_t *status;   // [4]
-    uint32_t *counters; // [kMaxWorkers], zero between launches
-    float *partials;    // [kMaxWorkers][kPartialFloats]
+    uint32_t *counters; // [kMaxCtas], zero between launches
+    float *partials;    // [kMaxCtas][kPartialFloats]
 };
 
 constexpr size_t kScratchStatusBytes = 256;
-constexpr size_t kScratchCounterBytes = sizeof(uint32_t) * kMaxWorkers;
-constexpr size_t kScratchPartialBytes = sizeof(float) * (size_t)kMaxWorkers * kPartialFloats;
+constexpr size_t kScratchCounterBytes = sizeof(uint32_t) * kMaxCtas;
+constexpr size_t kScratchPartialBytes = sizeof(float) * (size_t)kMaxCtas * kPartialFloats;
 constexpr size_t kScratchBytes = kScratchStatusBytes + kScratchCounterBytes + kScratchPartialBytes;
 
 inline Scratch scratch_from_base(void *base)
@@ -70,56 +70,20 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float lds_f32(uint32_t a)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float2 lds_f32x2(uint32_t a)
-{
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ float4 lds_f32x4(uint32_t a)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
-{
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ void sts_f32(uint32_t a, float v)
-{
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
-}
-__device__ __forceinline__ void sts_f32x2(uint32_t a, float x, float y)
-{
-    asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(a), "f"(x), "f"(y));
-}
-__device__ __forceinline__ void sts_f32x4(uint32_t a, float x, float y, float z, float w)
-{
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w));
-}
-
 // Position of the most significant set bit, or -1 (0xFFFFFFFF) for zero.
 __device__ __forceinline__ int bfind_u32(uint32_t m)
 {
     int r;
     asm("bfind.u32 %0, %1;" : "=r"(r) : "r"(m));
+    return r;
+}
+
+// 1 << s with the PTX rule for large shifts: s >= 32 (including -1 read as
+// unsigned) gives 0.
+__device__ __forceinline__ uint32_t bit_at(int s)
+{
+    uint32_t r;
+    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(1u), "r"(s));
     return r;
 }
 

@@ -10,158 +10,36 @@
 // which visits the same (column, value) pairs in reverse order with a
 // shorter dependency chain (bfind, clear) -- the product is the same sum.
 //
-// Main kernel (K % 128 == 0): the work is cut into units of 32 rows x 128
-// columns (4 mask words per row). Every warp is a stream-K worker that owns a
-// contiguous range of units, so all warps of the GPU get the same number of
-// weight bytes whatever the shape. Each warp runs its own TMA pipeline: NBUF
-// stage buffers in shared memory, each filled by three tensor copies (values
-// with 128-byte swizzle, masks, and the unit's 128-column slice of x) that
-// complete on one mbarrier. Lane i of the warp owns row i of the unit, so all
-// 32 lanes read x inside the same 32-column window: the gathers never
-// conflict in shared memory. A row block split between workers is finished
-// by whichever worker arrives last (a counter per block in the scratch), which
-// adds the partial sums in worker order: the result does not depend on timing.
+// Main kernel (K % 128 == 0): the stream-K TMA driver of streamk.cuh with
+// units of 32 rows x 128 columns (4 mask words per row). A stage is filled by
+// three tensor copies: values (box 64 x 32 bf16, 128-byte swizzle), masks
+// (box 4 x 32 u32) and the unit's 128-column slice of x (box 128 x batch).
+//
+// Lane i of a warp owns row i of the unit, so all 32 lanes read x inside the
+// same 32-column window. At batch 1 lane j holds column j of that window in a
+// register and the gather is a warp shuffle; at batch > 1 the window is
+// converted to fp32 [column][batch] in shared memory and the gather is one
+// conflict-free shared load per column.
 //
 // Fallback kernel (any K % 32 == 0): the same lane-per-row walk with plain
 // loads from global memory.
-#include <algorithm>
-#include <mutex>
-
-#include "kernels.h"
+#include "streamk.cuh"
 
 namespace nm {
 
-constexpr int kUnitRows = 32;                        // one row per lane
-constexpr int kUnitCols = 128;                       // columns per unit
-constexpr int kUnitWords = kUnitCols / 32;           // mask words per row per unit
-constexpr int kValBytes = kUnitRows * kUnitCols;     // 32 rows x 64 bf16
-constexpr int kMaskBytes = kUnitRows * kUnitWords * 4;
-constexpr int kGuardBytes = 64; // read by the walk of a malformed (all-clear) word
+constexpr int kSpCols = 128;                    // columns per unit
+constexpr int kSpWords = kSpCols / 32;          // mask words per row per unit
+constexpr int kValBytes = kUnitRows * kSpCols;  // 32 rows x 64 bf16
+constexpr int kMaskBytes = kUnitRows * kSpWords * 4;
 
-template <int B> struct BatchPad {
-    static constexpr int value = B == 1 ? 1 : B == 2 ? 2 : B <= 4 ? 4 : 8;
-};
-template <int B> constexpr int stage_bytes() { return (kValBytes + kMaskBytes + 256 * B + 1023) / 1024 * 1024; }
-template <int B> constexpr int xf_bytes() { return kUnitCols * BatchPad<B>::value * 4; }
-template <int B, int W, int NBUF> constexpr int tma_smem_bytes()
+// Load this lane's 4 mask words and 4 x 16 kept values of one unit.
+__device__ __forceinline__ void load_row_unit(const uint8_t *st, int lane, uint32_t (&m)[4], uint32_t (&v)[4][8])
 {
-    return 1024 + W * NBUF * stage_bytes<B>() + W * (kGuardBytes + xf_bytes<B>());
-}
-
-// Warps per CTA and stage buffers per warp, by batch size.
-template <int B> struct TmaCfg {
-    static constexpr int W = B <= 2 ? 16 : B <= 4 ? 12 : 8;
-    static constexpr int NBUF = 2;
-};
-
-struct SpmvParams {
-    void *y;      // bf16 or fp32 [batch][rows]
-    int64_t rows; // valid rows
-    int64_t U;    // units = row_blocks * KC
-    int32_t KC;   // units per row block (K / 128)
-    int32_t G;    // stream-K workers (warps) with work, G <= U
-    Scratch scratch;
-};
-
-template <int B, bool F32OUT>
-__device__ __forceinline__ void store_y(void *y, int64_t rows, int64_t row, const float (&v)[B])
-{
-    if (row >= rows)
-        return;
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-        if (F32OUT)
-            ((float *)y)[(int64_t)b * rows + row] = v[b];
-        else
-            ((uint16_t *)y)[(int64_t)b * rows + row] = f32_to_bf16_rn(v[b]);
-    }
-}
-
-// Worker whose unit range contains unit u (ranges are [U*g/G, U*(g+1)/G)).
-__device__ __forceinline__ int64_t owner_of(int64_t u, int64_t U, int64_t G)
-{
-    return ((u + 1) * G - 1) / U;
-}
-
-// Finish row block rb after this worker has covered units [s0, s1) of it.
-template <int B, bool F32OUT>
-__device__ __forceinline__ void finish_row_block(const SpmvParams &p, int64_t g, int64_t rb0, int64_t rb,
-                                                 int64_t s0, int64_t s1, const float (&tot)[B], int lane)
-{
-    const int64_t KC = p.KC;
-    const int64_t row = rb * kUnitRows + lane;
-    if (s0 == rb * KC && s1 == (rb + 1) * KC) {
-        store_y<B, F32OUT>(p.y, p.rows, row, tot);
-        return;
-    }
-    const int64_t G = p.G, U = p.U;
-    const int64_t first = owner_of(rb * KC, U, G);
-    const int64_t last = owner_of((rb + 1) * KC - 1, U, G);
-    const int slot = (rb == rb0) ? 0 : 1;
-    float *mine = p.scratch.partials + ((g * 2 + slot) * 32 + lane) * 8;
-#pragma unroll
-    for (int b = 0; b < B; ++b)
-        mine[b] = tot[b];
-    __threadfence();
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0)
-        old = atomicAdd(&p.scratch.counters[first], 1u);
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    if (old != (uint32_t)(last - first))
-        return;
-    // Last contributor: add every contributor's partial in worker order.
-    __threadfence();
-    float sum[B];
-#pragma unroll
-    for (int b = 0; b < B; ++b)
-        sum[b] = 0.f;
-    for (int64_t c = first; c <= last; ++c) {
-        const int64_t c_rb0 = (U * c / G) / KC;
-        const int cs = (rb == c_rb0) ? 0 : 1;
-        const float *q = p.scratch.partials + ((c * 2 + cs) * 32 + lane) * 8;
-#pragma unroll
-        for (int b = 0; b < B; ++b)
-            sum[b] += ldcg_f32(q + b);
-    }
-    store_y<B, F32OUT>(p.y, p.rows, row, sum);
-    if (lane == 0)
-        atomicExch(&p.scratch.counters[first], 0u);
-}
-
-// x slice of one unit, bf16 [B][128] -> fp32 [128][BP] in the warp's buffer.
-template <int B>
-__device__ __forceinline__ void convert_x(const uint8_t *sx, uint8_t *xf, int lane)
-{
-    constexpr int BP = BatchPad<B>::value;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int c = lane + 32 * i;
-        float f[BP];
-#pragma unroll
-        for (int b = 0; b < BP; ++b)
-            f[b] = (b < B) ? bf16_to_f32(*(const uint16_t *)(sx + b * 256 + c * 2)) : 0.f;
-        float *dst = (float *)(xf + c * BP * 4);
-        if (BP == 1) {
-            dst[0] = f[0];
-        } else if (BP == 2) {
-            *(float2 *)dst = make_float2(f[0], f[1 % BP]);
-        } else {
-#pragma unroll
-            for (int b = 0; b < BP; b += 4)
-                *(float4 *)(dst + b) = make_float4(f[b], f[(b + 1) % BP], f[(b + 2) % BP], f[(b + 3) % BP]);
-        }
-    }
-}
-
-// 16 fixed steps over the 4 mask words of this lane's row in one unit.
-template <int B>
-__device__ __forceinline__ void walk_unit(const uint8_t *st, const uint8_t *xf, int lane, float (&acc)[4][B])
-{
-    constexpr int BP = BatchPad<B>::value;
     const uint4 mw = *(const uint4 *)(st + kValBytes + lane * 16);
-    uint32_t m[4] = {mw.x, mw.y, mw.z, mw.w};
-    uint32_t v[4][8];
+    m[0] = mw.x;
+    m[1] = mw.y;
+    m[2] = mw.z;
+    m[3] = mw.w;
     const uint8_t *rowv = st + lane * 128;
     const int sw = lane & 7; // 128-byte swizzle: 16-byte chunk c of row r sits at c ^ (r & 7)
 #pragma unroll
@@ -175,33 +53,162 @@ __device__ __forceinline__ void walk_unit(const uint8_t *st, const uint8_t *xf, 
             v[q][4 * h + 3] = t.w;
         }
     }
+}
+
+// Batch 1: 16 fixed steps over the 4 words, x gathered by warp shuffle.
+// Each word is walked from both ends at once: step j takes the highest
+// remaining set bit for value 15-j and the lowest remaining set bit for value
+// j. The two walks touch disjoint bits, so they are independent dependency
+// chains (the walk is bound by the latency of find-bit -> clear, not by
+// issue), and each step's two products go through one packed fp32x2 FMA.
+__device__ __forceinline__ void walk_unit_b1(const uint8_t *st, int lane, float (&acc)[4][1])
+{
+    uint32_t m[4], v[4][8];
+    load_row_unit(st, lane, m, v);
+    const uint8_t *sx = st + kValBytes + kMaskBytes;
+    float xr[4];
 #pragma unroll
-    for (int step = 0; step < 16; ++step) {
-        const int k = 15 - step; // value index of the highest remaining set bit
+    for (int q = 0; q < 4; ++q)
+        xr[q] = bf16_to_f32(*(const uint16_t *)(sx + (32 * q + lane) * 2));
+    uint32_t mh[4], ml[4];
+    float2 a2[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        mh[q] = m[q];
+        ml[q] = m[q];
+        a2[q] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int pos = bfind_u32(m[q]); // -1 only for a malformed word
-            m[q] &= ~(1u << (pos & 31));
-            const float *xa = (const float *)(xf + (q * 32 + pos) * BP * 4);
-            const uint32_t pr = v[q][k >> 1];
-            const float wv = (k & 1) ? bf16hi_to_f32(pr) : bf16lo_to_f32(pr);
-            if (BP == 1) {
-                acc[q][0] = fmaf(wv, xa[0], acc[q][0]);
-            } else if (BP == 2) {
-                const float2 xv = *(const float2 *)xa;
-                acc[q][0] = fmaf(wv, xv.x, acc[q][0]);
-                if (B > 1)
-                    acc[q][1 % B] = fmaf(wv, xv.y, acc[q][1 % B]);
-            } else {
+            const int ph = bfind_u32(mh[q]); // column of value 15-j (-1 only for a malformed word)
+            mh[q] ^= bit_at(ph);
+            const uint32_t t = ml[q] - 1u;
+            const int pl = bfind_u32(ml[q] ^ t); // column of value j: the lowest set bit
+            ml[q] &= t;
+            const float2 xv = make_float2(__shfl_sync(0xFFFFFFFFu, xr[q], ph), // lane index taken mod 32
+                                          __shfl_sync(0xFFFFFFFFu, xr[q], pl));
+            const int kh = 15 - j, kl = j;
+            const float wh = (kh & 1) ? bf16hi_to_f32(v[q][kh >> 1]) : bf16lo_to_f32(v[q][kh >> 1]);
+            const float wl = (kl & 1) ? bf16hi_to_f32(v[q][kl >> 1]) : bf16lo_to_f32(v[q][kl >> 1]);
+            a2[q] = __ffma2_rn(make_float2(wh, wl), xv, a2[q]);
+        }
+    }
 #pragma unroll
-                for (int b0 = 0; b0 < BP; b0 += 4) {
-                    if (b0 < B) {
-                        const float4 xv = *(const float4 *)(xa + b0);
-                        const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+    for (int q = 0; q < 4; ++q)
+        acc[q][0] += a2[q].x + a2[q].y;
+}
+
+// Byte tables for byte-regular words. When every byte of a mask word has
+// exactly four set bits -- always so for 2:4 and 4:8, whose M-subgroups sit
+// inside a byte -- the kept values of byte b are values 4b..4b+3 of the word,
+// so their columns can be looked up instead of walked: table b maps a byte
+// value to four bytes 8b + (position of its k-th set bit), k = 0..3, which are
+// directly the shuffle source lanes. A byte without four set bits maps to
+// kIrregular (bit 7 of byte 0), which no regular entry has.
+constexpr uint32_t kIrregular = 0x80u;
+constexpr int kLutBytes = 4 * 256 * 4;
+
+__device__ __forceinline__ void init_byte_tables(uint32_t *lut, int tid, int nthreads)
+{
+    for (int i = tid; i < 4 * 256; i += nthreads) {
+        const int b = i >> 8, e = i & 255;
+        uint32_t ent = kIrregular;
+        if (__popc(e) == 4) {
+            ent = 0;
+            int k = 0;
+            for (int j = 0; j < 8; ++j)
+                if ((e >> j) & 1)
+                    ent |= (uint32_t)(8 * b + j) << (8 * k++);
+        }
+        lut[i] = ent;
+    }
+}
+
+// Batch 1, byte-regular words: looked-up columns, x gathered by warp shuffle
+// (a shuffle uses the low 5 bits of its source lane, so the other bytes of a
+// table entry need no masking). Returns false, having accumulated nothing, if
+// any lane of the warp holds a word that is not byte-regular.
+__device__ __forceinline__ bool walk_unit_b1_lut(const uint8_t *st, const uint32_t *lut, int lane,
+                                                 float (&acc)[4][1])
+{
+    uint32_t m[4], v[4][8];
+    load_row_unit(st, lane, m, v);
+    uint32_t ent[4][4];
+    uint32_t flags = 0;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (b0 + j < B)
-                                acc[q][(b0 + j) % B] = fmaf(wv, xs[j], acc[q][(b0 + j) % B]);
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            ent[q][b] = lut[b * 256 + ((m[q] >> (8 * b)) & 0xFFu)];
+            flags |= ent[q][b];
+        }
+    if (!__all_sync(0xFFFFFFFFu, (flags & kIrregular) == 0))
+        return false;
+    const uint8_t *sx = st + kValBytes + kMaskBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float xr = bf16_to_f32(*(const uint16_t *)(sx + (32 * q + lane) * 2));
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t e = ent[q][b];
+            const uint32_t p0 = v[q][2 * b], p1 = v[q][2 * b + 1];
+            a0 = fmaf(bf16lo_to_f32(p0), __shfl_sync(0xFFFFFFFFu, xr, (int)e), a0);
+            a1 = fmaf(bf16hi_to_f32(p0), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 8)), a1);
+            a0 = fmaf(bf16lo_to_f32(p1), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 16)), a0);
+            a1 = fmaf(bf16hi_to_f32(p1), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 24)), a1);
+        }
+        acc[q][0] += a0 + a1;
+    }
+    return true;
+}
+
+// Batch > 1: the same two-ended walk, x from the fp32 [column][batch] window.
+template <int B>
+__device__ __forceinline__ void walk_unit_bn(const uint8_t *st, const uint8_t *xf, int lane, float (&acc)[4][B])
+{
+    constexpr int BP = BatchPad<B>::value;
+    uint32_t m[4], v[4][8];
+    load_row_unit(st, lane, m, v);
+    uint32_t mh[4], ml[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        mh[q] = m[q];
+        ml[q] = m[q];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int ph = bfind_u32(mh[q]); // -1 only for a malformed word: reads the guard band
+            mh[q] ^= bit_at(ph);
+            const uint32_t t = ml[q] - 1u;
+            const int pl = bfind_u32(ml[q] ^ t);
+            ml[q] &= t;
+            const int kh = 15 - j, kl = j;
+            const float wh = (kh & 1) ? bf16hi_to_f32(v[q][kh >> 1]) : bf16lo_to_f32(v[q][kh >> 1]);
+            const float wl = (kl & 1) ? bf16hi_to_f32(v[q][kl >> 1]) : bf16lo_to_f32(v[q][kl >> 1]);
+#pragma unroll
+            for (int side = 0; side < 2; ++side) {
+                const float w = side ? wl : wh;
+                const float *xa = (const float *)(xf + (q * 32 + (side ? pl : ph)) * BP * 4);
+                if (BP == 2) {
+                    const float2 xv = *(const float2 *)xa;
+                    acc[q][0] = fmaf(w, xv.x, acc[q][0]);
+                    acc[q][1 % B] = fmaf(w, xv.y, acc[q][1 % B]);
+                } else {
+#pragma unroll
+                    for (int b0 = 0; b0 < BP; b0 += 4) {
+                        if (b0 < B) {
+                            const float4 xv = *(const float4 *)(xa + b0);
+                            const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                if (b0 + jj < B)
+                                    acc[q][(b0 + jj) % B] = fmaf(w, xs[jj], acc[q][(b0 + jj) % B]);
+                        }
                     }
                 }
             }
@@ -209,134 +216,59 @@ __device__ __forceinline__ void walk_unit(const uint8_t *st, const uint8_t *xf, 
     }
 }
 
-template <int B, int W, int NBUF, bool F32OUT>
-__global__ void __launch_bounds__(W * 32, 1)
-    spmv_tma_kernel(const __grid_constant__ CUtensorMap tm_vals, const __grid_constant__ CUtensorMap tm_masks,
-                    const __grid_constant__ CUtensorMap tm_x, const SpmvParams p)
-{
-    constexpr int SB = stage_bytes<B>();
-    constexpr uint32_t TX = kValBytes + kMaskBytes + 256 * B;
-    __shared__ __align__(8) uint64_t full_bar[W * NBUF];
-    extern __shared__ __align__(1024) uint8_t dsmem[];
+// The sparse unit: masks + values + x slice per stage.
+struct SparseUnit {
+    static constexpr int kCols = kSpCols;
+    static constexpr bool kHasMasks = true;
+    static constexpr int kXOffset = kValBytes + kMaskBytes;
+    template <int B> static constexpr int stage_bytes() { return (kXOffset + 2 * kCols * B + 1023) / 1024 * 1024; }
+    template <int B> static constexpr uint32_t tx_bytes() { return kXOffset + 2 * kCols * B; }
+    template <int B> static constexpr int xf_bytes() { return B == 1 ? 0 : kCols * BatchPad<B>::value * 4; }
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    uint8_t *const sbase = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
-    uint8_t *const stage0p = sbase + warp * NBUF * SB;
-    uint8_t *const xfp = sbase + W * NBUF * SB + warp * (kGuardBytes + xf_bytes<B>()) + kGuardBytes;
-    const uint32_t stage0 = smem_addr(stage0p);
-    const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
-
-    const int64_t g = (int64_t)blockIdx.x * W + warp;
-    if (g >= p.G) {
-        pdl_wait_upstream();
-        pdl_launch_dependents();
-        return;
+    static __device__ __forceinline__ void issue_weights(uint32_t st, uint32_t bar, int kc, int32_t row0,
+                                                         uint64_t pol, const TensorMaps &maps)
+    {
+        tma_load_2d_hint(st, &maps.w, kc * (kCols / 2), row0, bar, pol);
+        tma_load_2d_hint(st + kValBytes, &maps.m, kc * kSpWords, row0, bar, pol);
     }
-    const int64_t ub = p.U * g / p.G;
-    const int64_t ue = p.U * (g + 1) / p.G;
-    const int n = (int)(ue - ub);
-    const int64_t KC = p.KC;
-    const int64_t rb0 = ub / KC;
-    const int64_t kc0 = ub - rb0 * KC;
 
-    if (lane == 0) {
-        for (int i = 0; i < NBUF; ++i)
-            mbar_init(bar0 + 8 * i, 1);
-        fence_mbar_init();
+    static constexpr int kSharedBytes = kLutBytes;
+    // Per-warp state: whether to try the byte tables. A warp that meets a
+    // unit with an irregular word (8:16, 16:32 data) stops trying.
+    struct State {
+        bool try_lut;
+    };
+    static __device__ __forceinline__ State initial_state() { return State{true}; }
+    static __device__ __forceinline__ void init_shared(uint8_t *p, int tid, int nthreads)
+    {
+        init_byte_tables((uint32_t *)p, tid, nthreads);
     }
-    __syncwarp();
 
-    // Weights do not depend on the previous kernel: start streaming them now.
-    const uint64_t pol = l2_policy_evict_first();
-    const int npre = n < NBUF ? n : NBUF;
-    if (lane == 0) {
-        int64_t rb = rb0, kc = kc0;
-        for (int i = 0; i < npre; ++i) {
-            const uint32_t st = stage0 + i * SB, bar = bar0 + 8 * i;
-            mbar_arrive_expect_tx(bar, TX);
-            tma_load_2d_hint(st, &tm_vals, (int32_t)(kc * 64), (int32_t)(rb * kUnitRows), bar, pol);
-            tma_load_2d_hint(st + kValBytes, &tm_masks, (int32_t)(kc * kUnitWords), (int32_t)(rb * kUnitRows),
-                             bar, pol);
-            if (++kc == KC) {
-                kc = 0;
-                ++rb;
+    template <int B>
+    static __device__ __forceinline__ void consume(const uint8_t *stp, uint8_t *xf, const uint8_t *ps, State &stt,
+                                                   int lane, float (&acc)[4][B])
+    {
+        if constexpr (B == 1) {
+            if (stt.try_lut) {
+                if (walk_unit_b1_lut(stp, (const uint32_t *)ps, lane, acc))
+                    return;
+                stt.try_lut = false;
             }
+            walk_unit_b1(stp, lane, acc);
+        } else {
+            convert_x<B, kCols>(stp + kXOffset, xf, lane);
+            __syncwarp();
+            walk_unit_bn<B>(stp, xf, lane, acc);
         }
     }
-    // x may be the previous kernel's output.
-    pdl_wait_upstream();
-    if (lane == 0) {
-        int64_t kc = kc0;
-        for (int i = 0; i < npre; ++i) {
-            tma_load_2d(stage0 + i * SB + kValBytes + kMaskBytes, &tm_x, (int32_t)(kc * kUnitCols), 0,
-                        bar0 + 8 * i);
-            if (++kc == KC)
-                kc = 0;
-        }
-    }
-    pdl_launch_dependents();
+};
 
-    float acc[4][B];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int b = 0; b < B; ++b)
-            acc[q][b] = 0.f;
-
-    int64_t rb = rb0, kc = kc0;       // unit being consumed
-    int64_t prb = rb0, pkc = kc0;     // unit to prefetch next (i + NBUF)
-    for (int i = 0; i < npre; ++i) {
-        if (++pkc == KC) {
-            pkc = 0;
-            ++prb;
-        }
-    }
-    int64_t seg0 = ub;
-    bool dead = false;
-    for (int i = 0; i < n; ++i) {
-        const int s = i % NBUF;
-        const uint32_t st = stage0 + s * SB, bar = bar0 + 8 * s;
-        mbar_wait_bounded(bar, (uint32_t)((i / NBUF) & 1), p.scratch.status, dead);
-        const uint8_t *stp = stage0p + s * SB;
-        convert_x<B>(stp + kValBytes + kMaskBytes, xfp, lane);
-        __syncwarp();
-        walk_unit<B>(stp, xfp, lane, acc);
-        __syncwarp();
-        if (i + NBUF < n) {
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar, TX);
-                tma_load_2d_hint(st, &tm_vals, (int32_t)(pkc * 64), (int32_t)(prb * kUnitRows), bar, pol);
-                tma_load_2d_hint(st + kValBytes, &tm_masks, (int32_t)(pkc * kUnitWords),
-                                 (int32_t)(prb * kUnitRows), bar, pol);
-                tma_load_2d(st + kValBytes + kMaskBytes, &tm_x, (int32_t)(pkc * kUnitCols), 0, bar);
-            }
-            if (++pkc == KC) {
-                pkc = 0;
-                ++prb;
-            }
-        }
-        const int64_t u = ub + i;
-        const bool rb_end = (kc + 1 == KC);
-        if (rb_end || i == n - 1) {
-            float tot[B];
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                tot[b] = (acc[0][b] + acc[1][b]) + (acc[2][b] + acc[3][b]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    acc[q][b] = 0.f;
-            }
-            finish_row_block<B, F32OUT>(p, g, rb0, rb, seg0, u + 1, tot, lane);
-            seg0 = u + 1;
-        }
-        if (++kc == KC) {
-            kc = 0;
-            ++rb;
-        }
-    }
-}
+// Warps per CTA by batch size (2 stage buffers per warp, 2 CTAs per SM).
+template <int B> struct SparseCfg {
+    static constexpr int W = B <= 2 ? 8 : B <= 4 ? 6 : 4;
+    static constexpr int NBUF = 2;
+    static constexpr int MINB = 2;
+};
 
 // ---------------------------------------------------------------------------
 // Fallback: lane-per-row walk with plain global loads (any K % 32 == 0).
@@ -386,79 +318,28 @@ __global__ void __launch_bounds__(256)
 
 SpmvPath spmv_path(int64_t rows, int64_t K)
 {
-    if (K % kUnitCols == 0 && K > 0 && rows > 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF)
+    if (K % kSpCols == 0 && K > 0 && rows > 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF)
         return kSpmvTma;
     return kSpmvSimple;
-}
-
-static nm_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
-                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                           CUtensorMapSwizzle swz)
-{
-    EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn)
-        return NM_ERR_CUDA;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? NM_OK : NM_ERR_CUDA;
 }
 
 template <int B, bool F32OUT>
 static nm_status launch_tma(const uint32_t *masks, const void *values, const void *x, void *y, int64_t rows,
                             int64_t K, const LaunchCtx &ctx)
 {
-    constexpr int W = TmaCfg<B>::W, NBUF = TmaCfg<B>::NBUF;
-    constexpr int smem = tma_smem_bytes<B, W, NBUF>();
-    auto kern = spmv_tma_kernel<B, W, NBUF, F32OUT>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    });
-    if (attr_err != cudaSuccess)
-        return NM_ERR_CUDA;
-
-    CUtensorMap tv, tmk, tx;
+    TensorMaps maps;
     nm_status s;
-    if ((s = encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, values, (uint64_t)K / 2, (uint64_t)rows,
-                       (uint64_t)K, 64, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
+    if ((s = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, values, (uint64_t)K / 2, (uint64_t)rows,
+                       (uint64_t)K, kSpCols / 2, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
         return s;
-    if ((s = encode_2d(&tmk, CU_TENSOR_MAP_DATA_TYPE_UINT32, masks, (uint64_t)K / 32, (uint64_t)rows,
-                       (uint64_t)K / 8, kUnitWords, kUnitRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+    if ((s = encode_2d(&maps.m, CU_TENSOR_MAP_DATA_TYPE_UINT32, masks, (uint64_t)K / 32, (uint64_t)rows,
+                       (uint64_t)K / 8, kSpWords, kUnitRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
         return s;
-    if ((s = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
-                       kUnitCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+    if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
+                       kSpCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
         return s;
-
-    SpmvParams p;
-    p.y = y;
-    p.rows = rows;
-    p.KC = (int32_t)(K / kUnitCols);
-    p.U = ((rows + kUnitRows - 1) / kUnitRows) * (int64_t)p.KC;
-    int64_t ctas = std::min<int64_t>((int64_t)ctx.num_sms, (p.U + W - 1) / W);
-    if (ctas < 1)
-        ctas = 1;
-    p.G = (int32_t)std::min<int64_t>(std::min<int64_t>(ctas * W, p.U), kMaxWorkers);
-    ctas = (p.G + W - 1) / W;
-    p.scratch = ctx.scratch;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(W * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = ctx.pdl ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tv, tmk, tx, p) != cudaSuccess)
-        return NM_ERR_CUDA;
-    return NM_OK;
+    return launch_streamk<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB, F32OUT>(
+        maps, y, rows, K / kSpCols, ctx);
 }
 
 template <int B, bool F32OUT>

@@ -94,6 +94,46 @@ def test_spmv_small_shapes(nm, rows, K, N, M):
         check_close(y32, ybf, y64, S, f"{rows}x{K} {N}:{M} b{batch}")
 
 
+# More row blocks than SMs, so CTAs share row blocks (stream-K fix-up across
+# CTAs), with 1, 3, 9 and 32 units per row block.
+STREAM_K_SHAPES = [(5000, 128), (10000, 128), (20000, 384), (4900, 4096), (9999, 1152), (6144, 4096)]
+
+
+@pytest.mark.parametrize("rows,K", STREAM_K_SHAPES)
+def test_spmv_stream_k_shapes(nm, rows, K):
+    for batch in (1, 2, 5):
+        _, masks, values, x, y64, S = oracle_case(rows, K, 8, 16, batch, seed=rows + K, select=False)
+        y32, ybf = run_spmv(nm, masks, values, x)
+        check_close(y32, ybf, y64, S, f"{rows}x{K} b{batch}")
+
+
+def test_spmv_mixed_patterns_in_one_matrix(nm):
+    """Row groups packed with different patterns: byte-regular words (2:4, 4:8)
+    and irregular ones (8:16, 16:32) in one matrix, interleaved at several
+    granularities, so warps meet both kinds of unit."""
+    K = 4096
+    parts = []
+    for i, (n, m_) in enumerate([(2, 4), (16, 32), (4, 8), (8, 16), (2, 4), (16, 32)]):
+        rows = [64, 96, 32, 160, 1000, 33][i]
+        parts.append((n, m_, to_bits(synth.nm_structured(rows, K, n, m_, seed=40 + i))))
+    Wp = np.concatenate([w for _, _, w in parts])
+    masks = np.concatenate([oracle.pack(w, n, m_)[0] for n, m_, w in parts])
+    values = np.concatenate([oracle.pack(w, n, m_)[1] for n, m_, w in parts])
+    x = to_bits(synth.activations(1, K, seed=41))
+    y64, S = oracle.spmv_f64(Wp, x)
+    y32, ybf = run_spmv(nm, masks, values, x)
+    check_close(y32, ybf, y64, S, "mixed patterns")
+
+
+@pytest.mark.parametrize("rows,K", STREAM_K_SHAPES)
+def test_dense_stream_k_shapes(nm, rows, K):
+    Wp = to_bits(synth.nm_structured(rows, K, 2, 4, seed=rows))
+    x = to_bits(synth.activations(3, K, seed=rows))
+    y64, S = oracle.spmv_f64(Wp, x)
+    y32 = nm.dense_gemv(dev(Wp), dev(x), f32=True).cpu().numpy()
+    check_close(y32, None, y64, S, f"dense {rows}x{K}")
+
+
 @pytest.mark.parametrize("batch", range(1, 9))
 def test_spmv_every_batch(nm, batch):
     for rows, K in ((96, 1024), (45, 96)):
