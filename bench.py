@@ -42,7 +42,7 @@ UNIT = "us/token"
 CONFIG_ID = 2  # stream-id namespace of the decode-token stack inputs
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "nm_spmv_llama8b_stack.txt")
-SPMV_SOURCE = os.path.join(ROOT, "sparse_decoding_gb300", "csrc", "spmv.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "sparse_decoding_gb300", "csrc", f) for f in ("spmv.cu", "streamk.cuh")]
 
 
 def parse_args():
@@ -297,7 +297,7 @@ def recorded_traffic():
             if ":" in line:
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-        sha = hashlib.sha256(open(SPMV_SOURCE, "rb").read()).hexdigest()
+        sha = hashlib.sha256(b"".join(open(f, "rb").read() for f in KERNEL_SOURCES)).hexdigest()
         if fields.get("kernel_source_sha256") != sha:
             return None
         return float(fields["dram_bytes_per_launch"])
@@ -499,7 +499,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": recorded_traffic(),
-                     "kernel": "spmv_tma_kernel",
+                     "kernel": "streamk_kernel<SparseUnit>",
                      "achieved_basis": f"{step_bytes} algorithmic bytes per step / {4 * layers} launches, "
                                        "over the event-timed step (gaps between launches included)"},
         "per_shape": per_shape,
