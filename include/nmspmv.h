@@ -172,6 +172,30 @@ nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream
 nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
 
 /*
+ * nm_spmv_noalloc -- nm_spmv for callers that cannot allocate device memory.
+ * The pages describe no such entry point; it exists for integration only.
+ * nm_spmv obtains its per-device scratch with cudaMalloc on first use. Code
+ * that runs inside another framework's memory pool, or under a rule that no
+ * allocation may happen outside it, cannot allow that. This call computes the
+ * same y (same kernel, same summation order) with its scratch in a fixed
+ * device array that is part of the loaded library: about 1 MB on every GPU
+ * that loads the library, held until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   Arguments, layouts and errors are those of nm_spmv. Asynchronous.
+ *   Limit: the array holds the scratch of 512 CTAs; on a device whose grid
+ *   would need more (over 256 SMs) the call returns NM_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call outside CUDA graph capture.
+ *   Every call on a device shares the one array and finds it as the previous
+ *   call left it; each call clears the counters it needs at its start. Calls
+ *   whose executions overlap on the GPU (other streams, or other host threads)
+ *   race on the array: serialize them. A bounded wait that runs out is not
+ *   reported by nm_device_status for this call.
+ */
+nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const void *x_bf16,
+                          void *y_bf16, int64_t rows, int64_t K, int batch, void *stream);
+
+/*
  * nm_device_status -- waits for `stream`, then returns and clears the status
  * word of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
  * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed).

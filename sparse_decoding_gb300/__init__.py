@@ -32,7 +32,7 @@ PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 # Every symbol the header declares (the CPU test checks they are exported).
 EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
-           "nm_device_status")
+           "nm_device_status", "nm_spmv_noalloc")
 
 
 class NmError(RuntimeError):
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         "nm_spmv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
         "dense_gemv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
         "nm_device_status": ([p], i32),
+        "nm_spmv_noalloc": ([p, p, p, p, i64, i64, i32, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)

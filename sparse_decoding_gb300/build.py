@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnmspmv.so")
 
-SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "pack_host.cpp"]
+SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "noalloc.cu", "pack_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -21,6 +21,9 @@ struct LaunchCtx {
 enum SpmvPath { kSpmvTma = 0, kSpmvSimple = 1 };
 SpmvPath spmv_path(int64_t rows, int64_t K);
 
+// Largest grid (CTAs) the SpMV launches on a device with `num_sms` SMs.
+int spmv_max_ctas(int num_sms);
+
 nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,
                       int64_t rows, int64_t K, int batch, const LaunchCtx &ctx);
 nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K,

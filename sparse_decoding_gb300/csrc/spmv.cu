@@ -316,6 +316,15 @@ __global__ void __launch_bounds__(256)
 // Host side
 // ---------------------------------------------------------------------------
 
+int spmv_max_ctas(int num_sms)
+{
+    int m = SparseCfg<1>::MINB;
+    m = std::max(m, SparseCfg<2>::MINB);
+    m = std::max(m, SparseCfg<4>::MINB);
+    m = std::max(m, SparseCfg<8>::MINB);
+    return std::min(num_sms * m, kMaxCtas);
+}
+
 SpmvPath spmv_path(int64_t rows, int64_t K)
 {
     if (K % kSpCols == 0 && K > 0 && rows > 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF)
