@@ -173,8 +173,13 @@ static nm_status launch_gemv_tma(const void *W, const void *x, void *y, int64_t 
     if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
                        kDnCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
         return s;
+    const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kDnCols;
+    if constexpr (B <= 2) {
+        if (nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
+            return launch_streamk<DenseUnit, B, 16, 2, 1, F32OUT>(maps, y, rows, KC, ctx);
+    }
     return launch_streamk<DenseUnit, B, DenseCfg<B>::W, DenseCfg<B>::NBUF, DenseCfg<B>::MINB, F32OUT>(
-        maps, y, rows, K / kDnCols, ctx);
+        maps, y, rows, KC, ctx);
 }
 
 template <int B, bool F32OUT>

@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(256)
 
 int spmv_max_ctas(int num_sms)
 {
-    int m = SparseCfg<1>::MINB;
+    int m = 1; // the 16-warp shape runs one CTA per SM
+    m = std::max(m, SparseCfg<1>::MINB);
     m = std::max(m, SparseCfg<2>::MINB);
     m = std::max(m, SparseCfg<4>::MINB);
     m = std::max(m, SparseCfg<8>::MINB);
@@ -347,8 +348,15 @@ static nm_status launch_tma(const uint32_t *masks, const void *values, const voi
     if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
                        kSpCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
         return s;
+    const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kSpCols;
+    if constexpr (B <= 2) {
+        // Few, long row blocks (at most one per SM, 64+ units each): one CTA
+        // of 16 warps per row block halves each warp's share of it.
+        if (nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
+            return launch_streamk<SparseUnit, B, 16, 2, 1, F32OUT>(maps, y, rows, KC, ctx);
+    }
     return launch_streamk<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB, F32OUT>(
-        maps, y, rows, K / kSpCols, ctx);
+        maps, y, rows, KC, ctx);
 }
 
 template <int B, bool F32OUT>

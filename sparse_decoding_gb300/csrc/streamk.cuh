@@ -51,10 +51,11 @@ struct TensorMaps {
 };
 
 struct StreamKParams {
-    void *y;      // bf16 or fp32 [batch][rows]
-    int64_t rows; // valid rows
-    int64_t U;    // units = row_blocks * KC
-    int32_t KC;   // units per row block
+    void *y;        // bf16 or fp32 [batch][rows]
+    int64_t rows;   // valid rows
+    int64_t U;      // units = row_blocks * KC
+    int32_t KC;     // units per row block
+    int32_t whole;  // CTA ranges in whole row blocks (no row block shared by CTAs)
     Scratch scratch;
 };
 
@@ -217,8 +218,14 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
     const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
 
     CtaRange cr;
-    cr.cs = muldiv(p.U, blockIdx.x, gridDim.x);
-    cr.ce = muldiv(p.U, blockIdx.x + 1, gridDim.x);
+    if (p.whole) {
+        const int64_t nrb = p.U / p.KC;
+        cr.cs = muldiv(nrb, blockIdx.x, gridDim.x) * p.KC;
+        cr.ce = muldiv(nrb, blockIdx.x + 1, gridDim.x) * p.KC;
+    } else {
+        cr.cs = muldiv(p.U, blockIdx.x, gridDim.x);
+        cr.ce = muldiv(p.U, blockIdx.x + 1, gridDim.x);
+    }
     cr.nw = (int)((cr.ce - cr.cs) < W ? (cr.ce - cr.cs) : W);
 
     Pol::init_shared(pol_smem, threadIdx.x, W * 32);
@@ -356,15 +363,42 @@ inline nm_status encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void 
     return r == CUDA_SUCCESS ? NM_OK : NM_ERR_CUDA;
 }
 
+// How a launch splits its row blocks over CTAs.
+struct Split {
+    int64_t ctas;
+    bool whole; // every CTA owns whole row blocks
+};
+
+// Whole row blocks per CTA avoid the fix-up between CTAs: at the end of a
+// kernel, a row block shared by CTAs costs a chain of dependent L2 round trips
+// (publish, count, read back) that delays the kernel's completion -- and with
+// it the next kernel -- by several microseconds. Take whole row blocks when
+// that keeps the CTAs within ~15% of even work and gives no warp more than
+// about three units beyond an even split over all slots (the fix-up costs
+// about that much); otherwise split units evenly (stream-K) over all slots.
+inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
+{
+    const int64_t slots = (int64_t)num_sms * minb;
+    const int64_t U = nrb * KC;
+    Split sp;
+    sp.ctas = std::min<int64_t>(nrb, slots);
+    const int64_t most = (nrb + sp.ctas - 1) / sp.ctas; // row blocks of the busiest CTA
+    const bool balanced = most * sp.ctas <= nrb + nrb / 7;
+    const int64_t per_warp_whole = (most * KC + W - 1) / W;
+    const int64_t per_warp_even = (U + slots * W - 1) / (slots * W);
+    sp.whole = balanced && per_warp_whole <= per_warp_even + 3;
+    if (!sp.whole)
+        sp.ctas = std::max<int64_t>(1, std::min<int64_t>(slots, U / kMinUnitsPerCta));
+    sp.ctas = std::min<int64_t>(sp.ctas, kMaxCtas);
+    return sp;
+}
+
 // Launch the stream-K kernel for a problem of `rows` rows and KC units per row
 // block. MINB CTAs of W warps share an SM, so that at a kernel boundary the
 // next kernel's CTAs can take the place of this kernel's first finishers and
 // start streaming their weights while the rest of this kernel drains.
-// `whole_rb`: when there are at most MINB x SMs row blocks, give every CTA whole
-// row blocks (no fix-up between CTAs) instead of splitting over all slots.
 template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
-nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t KC, const LaunchCtx &ctx,
-                         bool whole_rb = false)
+nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t KC, const LaunchCtx &ctx)
 {
     constexpr int smem = streamk_smem_bytes<Pol, B, W, NBUF>();
     static_assert(MINB * (smem + 1024) <= 232448, "MINB CTAs must fit one SM's shared memory");
@@ -384,15 +418,9 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     p.U = ((rows + kUnitRows - 1) / kUnitRows) * KC;
     p.scratch = ctx.scratch;
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows;
-    const int64_t slots = (int64_t)ctx.num_sms * MINB;
-    // Whole row blocks per CTA avoid the fix-up between CTAs (a few dependent
-    // L2 round trips at the end of the kernel) but may give each warp more
-    // units than an even split; take them while that costs at most about as
-    // much as the fix-up (~3 units of work).
-    if (nrb <= slots && (KC + W - 1) / W <= (p.U + slots * W - 1) / (slots * W) + 3)
-        whole_rb = true;
-    int64_t ctas = (whole_rb && nrb <= slots) ? nrb : std::min<int64_t>(slots, p.U / kMinUnitsPerCta);
-    ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, kMaxCtas));
+    const Split sp = choose_split(nrb, KC, W, MINB, ctx.num_sms);
+    p.whole = sp.whole ? 1 : 0;
+    const int64_t ctas = sp.ctas;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);

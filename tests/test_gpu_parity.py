@@ -96,7 +96,9 @@ def test_spmv_small_shapes(nm, rows, K, N, M):
 
 # More row blocks than SMs, so CTAs share row blocks (stream-K fix-up across
 # CTAs), with 1, 3, 9 and 32 units per row block.
-STREAM_K_SHAPES = [(5000, 128), (10000, 128), (20000, 384), (4900, 4096), (9999, 1152), (6144, 4096)]
+STREAM_K_SHAPES = [(5000, 128), (10000, 128), (20000, 384), (4900, 4096), (9999, 1152), (6144, 4096),
+                   # few row blocks, long K: row blocks shared by many CTAs
+                   (64, 14336), (96, 28672), (33, 8192), (250, 4096), (1, 4096)]
 
 
 @pytest.mark.parametrize("rows,K", STREAM_K_SHAPES)
