@@ -110,20 +110,40 @@ __device__ __forceinline__ void walk_unit_b1(const uint8_t *st, int lane, float 
 constexpr uint32_t kIrregular = 0x80u;
 constexpr int kLutBytes = 4 * 256 * 4;
 
+// The four tables, computed at compile time into the library image. Copied
+// with 16-byte loads, so the object is 16-byte aligned.
+struct alignas(16) ByteTables {
+    uint32_t v[4 * 256];
+    constexpr ByteTables() : v()
+    {
+        for (int i = 0; i < 4 * 256; ++i) {
+            const int b = i >> 8, e = i & 255;
+            int bits = 0;
+            for (int j = 0; j < 8; ++j)
+                bits += (e >> j) & 1;
+            uint32_t ent = kIrregular;
+            if (bits == 4) {
+                ent = 0;
+                int k = 0;
+                for (int j = 0; j < 8; ++j)
+                    if ((e >> j) & 1) {
+                        ent |= (uint32_t)(8 * b + j) << (8 * k);
+                        ++k;
+                    }
+            }
+            v[i] = ent;
+        }
+    }
+};
+static_assert(alignof(ByteTables) == 16 && sizeof(ByteTables) == kLutBytes, "table layout");
+__device__ const ByteTables kByteTables{};
+
+// Copy the tables into the CTA's shared memory (16 bytes per thread-step;
+// `lut` is 16-byte aligned).
 __device__ __forceinline__ void init_byte_tables(uint32_t *lut, int tid, int nthreads)
 {
-    for (int i = tid; i < 4 * 256; i += nthreads) {
-        const int b = i >> 8, e = i & 255;
-        uint32_t ent = kIrregular;
-        if (__popc(e) == 4) {
-            ent = 0;
-            int k = 0;
-            for (int j = 0; j < 8; ++j)
-                if ((e >> j) & 1)
-                    ent |= (uint32_t)(8 * b + j) << (8 * k++);
-        }
-        lut[i] = ent;
-    }
+    for (int i = tid; i < kLutBytes / 16; i += nthreads)
+        ((uint4 *)lut)[i] = ((const uint4 *)kByteTables.v)[i];
 }
 
 // Batch 1, byte-regular words: looked-up columns, x gathered by warp shuffle

@@ -83,6 +83,14 @@ __device__ __forceinline__ int64_t muldiv(int64_t a, int64_t b, int64_t c)
     return (int64_t)(prod / (uint64_t)c);
 }
 
+// a / b for non-negative operands, with a 32-bit division when both fit.
+__device__ __forceinline__ int64_t div64(int64_t a, int64_t b)
+{
+    if (((uint64_t)a | (uint64_t)b) <= 0xFFFFFFFFull)
+        return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 // The CTA's place in the stream-K split.
 struct CtaRange {
     int64_t cs, ce; // unit range [cs, ce) of this CTA
@@ -108,9 +116,9 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
     }
     const int64_t U = p.U, P = gridDim.x;
     const int64_t c = blockIdx.x;
-    const int64_t first = (muldiv(rb_lo + 1, P, 1) - 1) / U;
-    const int64_t last = (muldiv(rb_hi, P, 1) - 1) / U;
-    const int slot = (rb == cr.cs / KC) ? 0 : 1;
+    const int64_t first = div64(((rb_lo + 1) * (P)) - 1, U);
+    const int64_t last = div64(((rb_hi) * (P)) - 1, U);
+    const int slot = (rb == div64(cr.cs, KC)) ? 0 : 1;
     float *mine = p.scratch.partials + (c * 2 + slot) * (8 * 32) + lane;
 #pragma unroll
     for (int b = 0; b < B; ++b)
@@ -135,7 +143,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
         for (int j = 0; j < 4; ++j) {
             const int64_t cc = c0 + j;
             if (cc <= last) {
-                const int cslot = (rb == muldiv(U, cc, P) / KC) ? 0 : 1;
+                const int cslot = (rb == div64(muldiv(U, cc, P), KC)) ? 0 : 1;
                 const float *q = p.scratch.partials + (cc * 2 + cslot) * (8 * 32) + lane;
 #pragma unroll
                 for (int b = 0; b < B; ++b)
@@ -173,14 +181,14 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
     if (s0 == rb_lo && s1 == rb_hi)
         return; // stored directly by the loop
     const int64_t n = cr.ce - cr.cs;
-    const int first = (int)((muldiv(lo - cr.cs + 1, cr.nw, 1) - 1) / n);
-    const int last = (int)((muldiv(hi - cr.cs, cr.nw, 1) - 1) / n);
+    const int first = (int)div64(((lo - cr.cs + 1) * (cr.nw)) - 1, n);
+    const int last = (int)div64(((hi - cr.cs) * (cr.nw)) - 1, n);
     float tot[B];
 #pragma unroll
     for (int b = 0; b < B; ++b)
         tot[b] = 0.f;
     for (int w = first; w <= last; ++w) {
-        const int64_t w_rb0 = (cr.cs + muldiv(n, w, cr.nw)) / KC;
+        const int64_t w_rb0 = div64(cr.cs + muldiv(n, w, cr.nw), KC);
         const int ws = (rb == w_rb0) ? 0 : 1;
         const float *q = part + ((w * 2 + ws) * B) * 32 + lane;
 #pragma unroll
@@ -193,7 +201,7 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
 template <class Pol, int B, int W, int NBUF> constexpr int streamk_smem_bytes()
 {
     return 1024 + W * NBUF * Pol::template stage_bytes<B>() + W * (kGuardBytes + Pol::template xf_bytes<B>()) +
-           W * part_bytes<B>() + W * 4 + Pol::kSharedBytes;
+           W * part_bytes<B>() + W * 4 + 16 + Pol::kSharedBytes;
 }
 
 template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
@@ -213,13 +221,14 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
     uint8_t *const xfp = sbase + W * NBUF * SB + warp * (kGuardBytes + XF) + kGuardBytes;
     float *const part = (float *)(sbase + W * NBUF * SB + W * (kGuardBytes + XF));
     uint32_t *const cnt = (uint32_t *)((uint8_t *)part + W * part_bytes<B>());
-    uint8_t *const pol_smem = (uint8_t *)(cnt + W);
+    // 16-byte aligned policy region (the tables are copied with 16-byte stores)
+    uint8_t *const pol_smem = (uint8_t *)(((uintptr_t)(cnt + W) + 15) & ~(uintptr_t)15);
     const uint32_t stage0 = smem_addr(stage0p);
     const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
 
     CtaRange cr;
     if (p.whole) {
-        const int64_t nrb = p.U / p.KC;
+        const int64_t nrb = div64(p.U, p.KC);
         cr.cs = muldiv(nrb, blockIdx.x, gridDim.x) * p.KC;
         cr.ce = muldiv(nrb, blockIdx.x + 1, gridDim.x) * p.KC;
     } else {
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
     const int64_t ue = active ? cr.cs + muldiv(n_cta, warp + 1, cr.nw) : 0;
     const int n = (int)(ue - ub);
     const int32_t KC = p.KC;
-    const int32_t rb0 = (int32_t)(ub / KC);
+    const int32_t rb0 = (int32_t)div64(ub, KC);
     const int32_t kc0 = (int32_t)(ub - (int64_t)rb0 * KC);
 
     // Weights do not depend on the previous kernel: start streaming them now.
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
     __syncthreads(); // every partial of this CTA is in shared memory
     if (n > 0) {
         // the first and the last segment are the only ones that can be partial
-        const int64_t rbf = rb0, rbl = (ue - 1) / KC;
+        const int64_t rbf = rb0, rbl = div64(ue - 1, KC);
         finish_in_cta<B, F32OUT>(p, cr, part, rbf, ub, rbf == rbl ? ue : (rbf + 1) * (int64_t)KC, lane);
         if (rbl != rbf)
             finish_in_cta<B, F32OUT>(p, cr, part, rbl, rbl * (int64_t)KC, ue, lane);
