@@ -172,6 +172,47 @@ nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream
 nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
 
 /*
+ * nm_stack_plan -- a decode-token stack prepared once, run many times.
+ * The linears, their order and the dependency rule are those of
+ * nm_spmv_stack / dense_gemv_stack: op i+1 reads its x only after every part
+ * of op i's y has been stored. Two ways to run it:
+ *   default: one kernel per op, chained with programmatic dependent launch
+ *     (as nm_spmv_stack; the fastest on GB300 for decode-sized ops);
+ *   NM_STACK_PERSISTENT: one persistent cooperative kernel walks all ops; a
+ *     grid-wide barrier stands in for each kernel boundary, and each warp
+ *     starts streaming the next op's weights before it arrives there. Used
+ *     only when every op is on the TMA path (sparse: K % 128 == 0; dense:
+ *     K % 64 == 0; rows, K > 0); otherwise the plan runs the default way.
+ *
+ * nm_stack_plan_create -- validates ops[0..n_ops) (host memory, read during
+ *   the call; each op as for nm_spmv, or dense_gemv with NM_STACK_DENSE, with
+ *   `batch` rows of x) and prepares the plan; with NM_STACK_PERSISTENT it
+ *   encodes every op's descriptors into device memory that the plan owns
+ *   (cudaMalloc; synchronous). The plan holds the ops' device pointers: the
+ *   buffers must stay allocated, and each run reads and writes whatever they
+ *   hold then. Make this call outside CUDA graph capture, on the device the
+ *   plan will run on. *plan is set on NM_OK only. Errors: those of the per-op
+ *   checks, NM_ERR_INVALID_ARG (NULL plan, n_ops < 0, unknown flag),
+ *   NM_ERR_CUDA.
+ * nm_stack_plan_run -- runs the plan on `stream` (asynchronous). The current
+ *   device must be the plan's (NM_ERR_INVALID_ARG otherwise). Runs of one
+ *   plan, and runs of different plans or other calls of this library on the
+ *   same device, must not overlap on the GPU (they share the per-device
+ *   scratch, and a persistent plan its barrier word). May be captured in a
+ *   CUDA graph. A bounded wait that runs out is reported by nm_device_status.
+ * nm_stack_plan_destroy -- frees the plan (waits for the device first);
+ *   NULL is accepted.
+ */
+typedef struct nm_stack_plan nm_stack_plan;
+
+#define NM_STACK_DENSE 1u      /* ops are dense GEMVs (W), not sparse SpMVs */
+#define NM_STACK_PERSISTENT 2u /* one persistent launch per run */
+
+nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsigned flags, nm_stack_plan **plan);
+nm_status nm_stack_plan_run(const nm_stack_plan *plan, void *stream);
+nm_status nm_stack_plan_destroy(nm_stack_plan *plan);
+
+/*
  * nm_spmv_noalloc -- nm_spmv for callers that cannot allocate device memory.
  * The pages describe no such entry point; it exists for integration only.
  * nm_spmv obtains its per-device scratch with cudaMalloc on first use. Code

@@ -29,10 +29,14 @@ NM_ERR_TIMEOUT = 7
 
 PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 
+NM_STACK_DENSE = 1
+NM_STACK_PERSISTENT = 2
+
 # Every symbol the header declares (the CPU test checks they are exported).
 EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
-           "nm_device_status", "nm_spmv_noalloc")
+           "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
+           "nm_stack_plan_destroy")
 
 
 class NmError(RuntimeError):
@@ -75,6 +79,9 @@ def lib() -> ctypes.CDLL:
         "dense_gemv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
         "nm_device_status": ([p], i32),
         "nm_spmv_noalloc": ([p, p, p, p, i64, i64, i32, p], i32),
+        "nm_stack_plan_create": ([ctypes.POINTER(NmLinear), i32, i32, ctypes.c_uint, ctypes.POINTER(p)], i32),
+        "nm_stack_plan_run": ([p, p], i32),
+        "nm_stack_plan_destroy": ([p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -219,15 +226,39 @@ def dense_gemv_stack(ops: Sequence[dict], batch: int) -> None:
 
 
 class StackPlan:
-    """A decode-token stack with its descriptor array built once; ``run()`` launches it."""
+    """A decode-token stack prepared once (``nm_stack_plan``); ``run()`` launches it.
 
-    def __init__(self, ops: Sequence[dict], batch: int, dense: bool = False):
-        self._keep = list(ops)  # keep the tensors alive as long as the plan
-        self._arr = _linear_array(self._keep)
-        self._n = len(self._keep)
+    By default each op is its own kernel, chained with programmatic dependent
+    launch; with ``persistent=True`` the whole stack is one persistent kernel
+    launch with a grid barrier between ops (when every op is on the TMA path).
+    The plan holds the ops' device pointers: it keeps their tensors alive
+    until ``close()``.
+    """
+
+    def __init__(self, ops: Sequence[dict], batch: int, dense: bool = False, persistent: bool = False):
+        self._keep = list(ops)
         self.batch = batch
-        self._fn = lib().dense_gemv_stack if dense else lib().nm_spmv_stack
-        self._name = "dense_gemv_stack" if dense else "nm_spmv_stack"
+        self.dense = dense
+        arr = _linear_array(self._keep)
+        flags = (NM_STACK_DENSE if dense else 0) | (NM_STACK_PERSISTENT if persistent else 0)
+        h = ctypes.c_void_p()
+        _check(lib().nm_stack_plan_create(arr, len(self._keep), batch, flags, ctypes.byref(h)),
+               "nm_stack_plan_create")
+        self._h = h
 
     def run(self) -> None:
-        _check(self._fn(self._arr, self._n, self.batch, ctypes.c_void_p(_stream())), self._name)
+        if self._h is None:
+            raise RuntimeError("StackPlan is closed")
+        _check(lib().nm_stack_plan_run(self._h, ctypes.c_void_p(_stream())), "nm_stack_plan_run")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None:
+            h, self._h = self._h, None
+            _check(lib().nm_stack_plan_destroy(h), "nm_stack_plan_destroy")
+            self._keep = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,8 +1,11 @@
 // api.cu -- the library's C entry points (declared in include/nmspmv.h):
 // argument checks, the per-device scratch, and dispatch to the kernels.
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "kernels.h"
+#include "streamk.cuh"
 
 namespace nm {
 
@@ -138,6 +141,20 @@ static nm_status gemv_impl(const void *W, const void *x, void *y, bool f32out, i
 
 using namespace nm;
 
+// A prepared decode-token stack (opaque in the C ABI).
+struct nm_stack_plan {
+    int dev = 0;
+    int batch = 1;
+    bool dense = false;
+    int n_ops = 0;
+    bool persistent = false;  // one launch of the stack kernel; otherwise chained launches
+    int ctas = 0;             // grid of the persistent launch
+    void *dmem = nullptr;     // StackOp[n_ops], then the grid-barrier counter
+    StackOp *ops_dev = nullptr;
+    uint32_t *gbar = nullptr;
+    std::vector<nm_linear> ops; // host copy for the chained path
+};
+
 extern "C" {
 
 int nm_abi_version(void) { return 1; }
@@ -267,6 +284,108 @@ nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *str
             return s;
     }
     return NM_OK;
+}
+
+nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsigned flags, nm_stack_plan **plan)
+{
+    if (!plan || n_ops < 0 || (n_ops > 0 && !ops) || (flags & ~(NM_STACK_DENSE | NM_STACK_PERSISTENT)))
+        return NM_ERR_INVALID_ARG;
+    const bool dense = (flags & NM_STACK_DENSE) != 0;
+    bool fits = n_ops > 0 && (flags & NM_STACK_PERSISTENT);
+    for (int i = 0; i < n_ops; ++i) {
+        const nm_linear &o = ops[i];
+        nm_status s = dense ? check_gemv_args(o.W, o.x, o.y, o.rows, o.K, batch)
+                            : check_spmv_args(o.masks, o.values, o.x, o.y, o.rows, o.K, batch);
+        if (s != NM_OK)
+            return s;
+        fits = fits && (dense ? gemv_tma_ok(o.rows, o.K) : (o.rows > 0 && o.K > 0 && spmv_path(o.rows, o.K) == kSpmvTma));
+    }
+    if (n_ops == 0 && (batch < 1 || batch > 8))
+        return NM_ERR_UNSUPPORTED;
+    LaunchCtx ctx;
+    nm_status s = device_ctx(nullptr, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    nm_stack_plan *pl = new (std::nothrow) nm_stack_plan;
+    if (!pl)
+        return NM_ERR_CUDA;
+    if (cudaGetDevice(&pl->dev) != cudaSuccess) {
+        delete pl;
+        return NM_ERR_CUDA;
+    }
+    pl->batch = batch;
+    pl->dense = dense;
+    pl->n_ops = n_ops;
+    pl->ops.assign(ops, ops + n_ops);
+    pl->persistent = fits;
+    if (fits) {
+        s = dense ? stack_grid_dense(batch, ctx.num_sms, &pl->ctas) : stack_grid_sparse(batch, ctx.num_sms, &pl->ctas);
+        std::vector<StackOp> host(n_ops);
+        for (int i = 0; i < n_ops && s == NM_OK; ++i)
+            s = dense ? stack_encode_dense(ops[i], batch, pl->ctas, &host[i])
+                      : stack_encode_sparse(ops[i], batch, pl->ctas, &host[i]);
+        const size_t desc_bytes = ((sizeof(StackOp) * n_ops + 255) / 256) * 256;
+        if (s == NM_OK && cudaMalloc(&pl->dmem, desc_bytes + 256) != cudaSuccess) {
+            pl->dmem = nullptr;
+            s = NM_ERR_CUDA;
+        }
+        if (s == NM_OK) {
+            pl->ops_dev = (StackOp *)pl->dmem;
+            pl->gbar = (uint32_t *)((char *)pl->dmem + desc_bytes);
+            if (cudaMemcpy(pl->ops_dev, host.data(), sizeof(StackOp) * n_ops, cudaMemcpyHostToDevice) != cudaSuccess ||
+                cudaMemset(pl->gbar, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+                s = NM_ERR_CUDA;
+        }
+        if (s != NM_OK) {
+            if (pl->dmem)
+                cudaFree(pl->dmem);
+            delete pl;
+            return s;
+        }
+    }
+    *plan = pl;
+    return NM_OK;
+}
+
+nm_status nm_stack_plan_run(const nm_stack_plan *plan, void *stream)
+{
+    if (!plan)
+        return NM_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return NM_ERR_CUDA;
+    if (dev != plan->dev)
+        return NM_ERR_INVALID_ARG;
+    if (!plan->persistent)
+        return plan->dense ? dense_gemv_stack(plan->ops.data(), plan->n_ops, plan->batch, stream)
+                           : nm_spmv_stack(plan->ops.data(), plan->n_ops, plan->batch, stream);
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    s = plan->dense ? stack_launch_dense(plan->ops_dev, plan->n_ops, plan->batch, plan->gbar, plan->ctas, ctx)
+                    : stack_launch_sparse(plan->ops_dev, plan->n_ops, plan->batch, plan->gbar, plan->ctas, ctx);
+    if (s == NM_OK && cudaGetLastError() != cudaSuccess)
+        s = NM_ERR_CUDA;
+    return s;
+}
+
+nm_status nm_stack_plan_destroy(nm_stack_plan *plan)
+{
+    if (!plan)
+        return NM_OK;
+    nm_status s = NM_OK;
+    if (plan->dmem) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(plan->dev);
+        if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(plan->dmem) != cudaSuccess)
+            s = NM_ERR_CUDA;
+        if (cur >= 0)
+            cudaSetDevice(cur);
+    }
+    delete plan;
+    return s;
 }
 
 nm_status nm_device_status(void *stream)

@@ -96,9 +96,9 @@ struct DenseUnit {
     static constexpr int kCols = kDnCols;
     static constexpr bool kHasMasks = false;
     static constexpr int kWBytes = kUnitRows * kCols * 2;
-    static constexpr int kXOffset = kWBytes;
-    template <int B> static constexpr int stage_bytes() { return (kXOffset + 2 * kCols * B + 1023) / 1024 * 1024; }
-    template <int B> static constexpr uint32_t tx_bytes() { return kXOffset + 2 * kCols * B; }
+    template <int B> static constexpr int stage_bytes() { return (kWBytes + 1023) / 1024 * 1024; }
+    template <int B> static constexpr int x_bytes() { return 2 * kCols * B; }
+    template <int B> static constexpr uint32_t tx_bytes() { return kWBytes + x_bytes<B>(); }
     template <int B> static constexpr int xf_bytes() { return kCols * BatchPad<B>::value * 4; }
 
     static __device__ __forceinline__ void issue_weights(uint32_t st, uint32_t bar, int kc, int32_t row0,
@@ -112,18 +112,29 @@ struct DenseUnit {
     static __device__ __forceinline__ State initial_state() { return State{}; }
     static __device__ __forceinline__ void init_shared(uint8_t *, int, int) {}
 
-    template <int B>
-    static __device__ __forceinline__ void consume(const uint8_t *stp, uint8_t *xf, const uint8_t *, State &, int lane,
-                                                   float (&acc)[4][B])
+    // One lane's row of the tile: 8 chunks of 8 bf16, in column order.
+    template <int B> struct Regs {
+        uint4 w[8];
+    };
+    template <int B> static __device__ __forceinline__ void load(const uint8_t *stp, int lane, Regs<B> &r)
     {
-        constexpr int BP = BatchPad<B>::value;
-        convert_x<B, kCols>(stp + kXOffset, xf, lane);
-        __syncwarp();
         const uint8_t *roww = stp + lane * 128;
         const int sw = lane & 7; // 16-byte chunk c of row r sits at c ^ (r & 7)
 #pragma unroll
+        for (int c = 0; c < 8; ++c)
+            r.w[c] = *(const uint4 *)(roww + ((c ^ sw) << 4));
+    }
+
+    template <int B>
+    static __device__ __forceinline__ void compute(const Regs<B> &r, const uint8_t *xs, uint8_t *xf, const uint8_t *,
+                                                   State &, int lane, float (&acc)[4][B])
+    {
+        constexpr int BP = BatchPad<B>::value;
+        convert_x<B, kCols>(xs, xf, lane);
+        __syncwarp();
+#pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 t = *(const uint4 *)(roww + ((c ^ sw) << 4));
+            const uint4 t = r.w[c];
             const uint32_t wp[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -160,18 +171,26 @@ template <int B> struct DenseCfg {
     static constexpr int MINB = 2;
 };
 
+// Tensor maps of one dense linear: W (box 64 x 32 bf16, 128-byte swizzle), x (box 64 x B).
+template <int B>
+static nm_status encode_dense_maps(const void *W, const void *x, int64_t rows, int64_t K, TensorMaps *maps)
+{
+    memset(&maps->m, 0, sizeof maps->m);
+    nm_status s;
+    if ((s = encode_2d(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2,
+                       kDnCols, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
+        return s;
+    return encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
+                     kDnCols, B, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <int B, bool F32OUT>
 static nm_status launch_gemv_tma(const void *W, const void *x, void *y, int64_t rows, int64_t K,
                                  const LaunchCtx &ctx)
 {
     TensorMaps maps;
-    memset(&maps.m, 0, sizeof maps.m);
-    nm_status s;
-    if ((s = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)rows, (uint64_t)K * 2,
-                       kDnCols, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
-        return s;
-    if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
-                       kDnCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+    nm_status s = encode_dense_maps<B>(W, x, rows, K, &maps);
+    if (s != NM_OK)
         return s;
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kDnCols;
     if constexpr (B <= 2) {
@@ -225,6 +244,42 @@ static nm_status gemv_dispatch(const void *W, const void *x, void *y, int64_t ro
         return NM_ERR_UNSUPPORTED;
     }
 #undef NM_CASE
+}
+
+// ---------------------------------------------------------------------------
+// The persistent stack kernel over dense linears
+// ---------------------------------------------------------------------------
+
+template <int B>
+using DenseStack = StackLauncher<DenseUnit, B, DenseCfg<B>::W, DenseCfg<B>::NBUF, DenseCfg<B>::MINB>;
+
+bool gemv_tma_ok(int64_t rows, int64_t K)
+{
+    return K > 0 && rows > 0 && K % kDnCols == 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF;
+}
+
+nm_status stack_grid_dense(int batch, int num_sms, int *ctas)
+{
+    return with_batch(batch, [&](auto bc) { return DenseStack<decltype(bc)::value>::grid(num_sms, ctas); });
+}
+
+nm_status stack_encode_dense(const nm_linear &op, int batch, int ctas, StackOp *out)
+{
+    return with_batch(batch, [&](auto bc) {
+        constexpr int B = decltype(bc)::value;
+        nm_status s = encode_dense_maps<B>(op.W, op.x, op.rows, op.K, &out->maps);
+        if (s == NM_OK)
+            DenseStack<B>::split(out, op.y, op.rows, op.K / kDnCols, ctas);
+        return s;
+    });
+}
+
+nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
+                             const LaunchCtx &ctx)
+{
+    return with_batch(batch, [&](auto bc) {
+        return DenseStack<decltype(bc)::value>::launch(ops, n_ops, gbar, ctas, ctx);
+    });
 }
 
 nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K, int batch,

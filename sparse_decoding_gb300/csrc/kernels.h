@@ -33,6 +33,23 @@ nm_status launch_select(const void *W, const float *a, int64_t rows, int64_t K, 
 nm_status launch_pack(const void *W, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
                       void *values, const LaunchCtx &ctx);
 
+// The persistent stack kernel: a whole decode-token stack in one launch
+// (spmv.cu for sparse linears, gemv.cu for dense ones). Only shapes on the
+// TMA path qualify (spmv_path == kSpmvTma, gemv_tma_ok).
+struct StackOp; // one op's descriptor in device memory (streamk.cuh)
+bool gemv_tma_ok(int64_t rows, int64_t K);
+// CTAs of the (cooperative) launch for this batch on a device of num_sms SMs.
+nm_status stack_grid_sparse(int batch, int num_sms, int *ctas);
+nm_status stack_grid_dense(int batch, int num_sms, int *ctas);
+// Descriptor of one op for a launch of `ctas` CTAs, written to host memory.
+nm_status stack_encode_sparse(const nm_linear &op, int batch, int ctas, StackOp *out);
+nm_status stack_encode_dense(const nm_linear &op, int batch, int ctas, StackOp *out);
+// One launch over ops[0..n_ops) (device memory); gbar: the grid-barrier counter.
+nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
+                              const LaunchCtx &ctx);
+nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
+                             const LaunchCtx &ctx);
+
 // Returns the driver's cuTensorMapEncodeTiled, or nullptr if unavailable.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,

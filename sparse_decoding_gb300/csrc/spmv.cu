@@ -61,11 +61,9 @@ __device__ __forceinline__ void load_row_unit(const uint8_t *st, int lane, uint3
 // j. The two walks touch disjoint bits, so they are independent dependency
 // chains (the walk is bound by the latency of find-bit -> clear, not by
 // issue), and each step's two products go through one packed fp32x2 FMA.
-__device__ __forceinline__ void walk_unit_b1(const uint8_t *st, int lane, float (&acc)[4][1])
+__device__ __forceinline__ void walk_unit_b1(const uint32_t (&m)[4], const uint32_t (&v)[4][8], const uint8_t *sx, int lane,
+                                             float (&acc)[4][1])
 {
-    uint32_t m[4], v[4][8];
-    load_row_unit(st, lane, m, v);
-    const uint8_t *sx = st + kValBytes + kMaskBytes;
     float xr[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -150,11 +148,9 @@ __device__ __forceinline__ void init_byte_tables(uint32_t *lut, int tid, int nth
 // (a shuffle uses the low 5 bits of its source lane, so the other bytes of a
 // table entry need no masking). Returns false, having accumulated nothing, if
 // any lane of the warp holds a word that is not byte-regular.
-__device__ __forceinline__ bool walk_unit_b1_lut(const uint8_t *st, const uint32_t *lut, int lane,
-                                                 float (&acc)[4][1])
+__device__ __forceinline__ bool walk_unit_b1_lut(const uint32_t (&m)[4], const uint32_t (&v)[4][8], const uint8_t *sx,
+                                                 const uint32_t *lut, int lane, float (&acc)[4][1])
 {
-    uint32_t m[4], v[4][8];
-    load_row_unit(st, lane, m, v);
     uint32_t ent[4][4];
     uint32_t flags = 0;
 #pragma unroll
@@ -166,7 +162,6 @@ __device__ __forceinline__ bool walk_unit_b1_lut(const uint8_t *st, const uint32
         }
     if (!__all_sync(0xFFFFFFFFu, (flags & kIrregular) == 0))
         return false;
-    const uint8_t *sx = st + kValBytes + kMaskBytes;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float xr = bf16_to_f32(*(const uint16_t *)(sx + (32 * q + lane) * 2));
@@ -187,11 +182,10 @@ __device__ __forceinline__ bool walk_unit_b1_lut(const uint8_t *st, const uint32
 
 // Batch > 1: the same two-ended walk, x from the fp32 [column][batch] window.
 template <int B>
-__device__ __forceinline__ void walk_unit_bn(const uint8_t *st, const uint8_t *xf, int lane, float (&acc)[4][B])
+__device__ __forceinline__ void walk_unit_bn(const uint32_t (&m)[4], const uint32_t (&v)[4][8], const uint8_t *xf, int lane,
+                                             float (&acc)[4][B])
 {
     constexpr int BP = BatchPad<B>::value;
-    uint32_t m[4], v[4][8];
-    load_row_unit(st, lane, m, v);
     uint32_t mh[4], ml[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -240,9 +234,9 @@ __device__ __forceinline__ void walk_unit_bn(const uint8_t *st, const uint8_t *x
 struct SparseUnit {
     static constexpr int kCols = kSpCols;
     static constexpr bool kHasMasks = true;
-    static constexpr int kXOffset = kValBytes + kMaskBytes;
-    template <int B> static constexpr int stage_bytes() { return (kXOffset + 2 * kCols * B + 1023) / 1024 * 1024; }
-    template <int B> static constexpr uint32_t tx_bytes() { return kXOffset + 2 * kCols * B; }
+    template <int B> static constexpr int stage_bytes() { return (kValBytes + kMaskBytes + 1023) / 1024 * 1024; }
+    template <int B> static constexpr int x_bytes() { return 2 * kCols * B; }
+    template <int B> static constexpr uint32_t tx_bytes() { return kValBytes + kMaskBytes + x_bytes<B>(); }
     template <int B> static constexpr int xf_bytes() { return B == 1 ? 0 : kCols * BatchPad<B>::value * 4; }
 
     static __device__ __forceinline__ void issue_weights(uint32_t st, uint32_t bar, int kc, int32_t row0,
@@ -264,21 +258,31 @@ struct SparseUnit {
         init_byte_tables((uint32_t *)p, tid, nthreads);
     }
 
+    // One lane's row of the unit: its 4 mask words and 4 x 16 kept values.
+    template <int B> struct Regs {
+        uint32_t m[4];
+        uint32_t v[4][8];
+    };
+    template <int B> static __device__ __forceinline__ void load(const uint8_t *stp, int lane, Regs<B> &r)
+    {
+        load_row_unit(stp, lane, r.m, r.v);
+    }
+
     template <int B>
-    static __device__ __forceinline__ void consume(const uint8_t *stp, uint8_t *xf, const uint8_t *ps, State &stt,
-                                                   int lane, float (&acc)[4][B])
+    static __device__ __forceinline__ void compute(const Regs<B> &r, const uint8_t *xs, uint8_t *xf,
+                                                   const uint8_t *ps, State &stt, int lane, float (&acc)[4][B])
     {
         if constexpr (B == 1) {
             if (stt.try_lut) {
-                if (walk_unit_b1_lut(stp, (const uint32_t *)ps, lane, acc))
+                if (walk_unit_b1_lut(r.m, r.v, xs, (const uint32_t *)ps, lane, acc))
                     return;
                 stt.try_lut = false;
             }
-            walk_unit_b1(stp, lane, acc);
+            walk_unit_b1(r.m, r.v, xs, lane, acc);
         } else {
-            convert_x<B, kCols>(stp + kXOffset, xf, lane);
+            convert_x<B, kCols>(xs, xf, lane);
             __syncwarp();
-            walk_unit_bn<B>(stp, xf, lane, acc);
+            walk_unit_bn<B>(r.m, r.v, xf, lane, acc);
         }
     }
 };
@@ -353,20 +357,30 @@ SpmvPath spmv_path(int64_t rows, int64_t K)
     return kSpmvSimple;
 }
 
+// Tensor maps of one sparse linear: values (box 64 x 32 bf16, 128-byte
+// swizzle), masks (box 4 x 32 u32), x (box 128 x B bf16).
+template <int B>
+static nm_status encode_sparse_maps(const uint32_t *masks, const void *values, const void *x, int64_t rows, int64_t K,
+                                    TensorMaps *maps)
+{
+    nm_status s;
+    if ((s = encode_2d(&maps->w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, values, (uint64_t)K / 2, (uint64_t)rows,
+                       (uint64_t)K, kSpCols / 2, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
+        return s;
+    if ((s = encode_2d(&maps->m, CU_TENSOR_MAP_DATA_TYPE_UINT32, masks, (uint64_t)K / 32, (uint64_t)rows,
+                       (uint64_t)K / 8, kSpWords, kUnitRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+        return s;
+    return encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
+                     kSpCols, B, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <int B, bool F32OUT>
 static nm_status launch_tma(const uint32_t *masks, const void *values, const void *x, void *y, int64_t rows,
                             int64_t K, const LaunchCtx &ctx)
 {
     TensorMaps maps;
-    nm_status s;
-    if ((s = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, values, (uint64_t)K / 2, (uint64_t)rows,
-                       (uint64_t)K, kSpCols / 2, kUnitRows, CU_TENSOR_MAP_SWIZZLE_128B)) != NM_OK)
-        return s;
-    if ((s = encode_2d(&maps.m, CU_TENSOR_MAP_DATA_TYPE_UINT32, masks, (uint64_t)K / 32, (uint64_t)rows,
-                       (uint64_t)K / 8, kSpWords, kUnitRows, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
-        return s;
-    if ((s = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)B, (uint64_t)K * 2,
-                       kSpCols, B, CU_TENSOR_MAP_SWIZZLE_NONE)) != NM_OK)
+    nm_status s = encode_sparse_maps<B>(masks, values, x, rows, K, &maps);
+    if (s != NM_OK)
         return s;
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kSpCols;
     if constexpr (B <= 2) {
@@ -422,6 +436,37 @@ static nm_status dispatch(const uint32_t *masks, const void *values, const void 
         return NM_ERR_UNSUPPORTED;
     }
 #undef NM_CASE
+}
+
+// ---------------------------------------------------------------------------
+// The persistent stack kernel over sparse linears
+// ---------------------------------------------------------------------------
+
+template <int B>
+using SparseStack = StackLauncher<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB>;
+
+nm_status stack_grid_sparse(int batch, int num_sms, int *ctas)
+{
+    return with_batch(batch, [&](auto bc) { return SparseStack<decltype(bc)::value>::grid(num_sms, ctas); });
+}
+
+nm_status stack_encode_sparse(const nm_linear &op, int batch, int ctas, StackOp *out)
+{
+    return with_batch(batch, [&](auto bc) {
+        constexpr int B = decltype(bc)::value;
+        nm_status s = encode_sparse_maps<B>(op.masks, op.values, op.x, op.rows, op.K, &out->maps);
+        if (s == NM_OK)
+            SparseStack<B>::split(out, op.y, op.rows, op.K / kSpCols, ctas);
+        return s;
+    });
+}
+
+nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
+                              const LaunchCtx &ctx)
+{
+    return with_batch(batch, [&](auto bc) {
+        return SparseStack<decltype(bc)::value>::launch(ops, n_ops, gbar, ctas, ctx);
+    });
 }
 
 nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,

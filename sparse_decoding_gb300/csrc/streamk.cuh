@@ -18,19 +18,29 @@
 // A unit policy `Pol` supplies the stage layout and the per-unit arithmetic:
 //   Pol::kCols            columns per unit
 //   Pol::kHasMasks        whether maps.m is used
-//   Pol::stage_bytes<B>() bytes of one stage (multiple of 1024)
-//   Pol::tx_bytes<B>()    bytes the stage's copies deliver
-//   Pol::kXOffset         offset of the x slice in the stage
+//   Pol::stage_bytes<B>() bytes of one weight stage (multiple of 1024)
+//   Pol::tx_bytes<B>()    bytes one unit's copies deliver (weights + x)
+//   Pol::x_bytes<B>()     bytes of one unit's x slice (multiple of 128)
 //   Pol::xf_bytes<B>()    per-warp scratch in shared memory (may be 0)
 //   Pol::kSharedBytes     CTA-wide shared memory of the policy (tables)
 //   Pol::init_shared(ptr, tid, nthreads)            fills it before the pipeline starts
 //   Pol::issue_weights(stage, bar, kc, rb, policy, maps)
-//   Pol::consume<B>(stage_ptr, xf_ptr, shared_ptr, state, lane, acc)
+//   Pol::Regs<B>          the unit's weights as one lane holds them
+//   Pol::load<B>(stage_ptr, lane, regs)             stage -> registers
+//   Pol::compute<B>(regs, x_ptr, xf_ptr, shared_ptr, state, lane, acc)
 //                         accumulates into acc[4][B]; `state` is per warp
+//
+// A unit's weights are copied from its stage into registers first; the stage
+// is then refilled at once, and the arithmetic runs while the refill is in
+// flight, so a stage is busy only for the memory round trip, not for the
+// round trip plus the arithmetic. The x slices have their own ring of NBUF+1
+// slots per warp, so the slice of the unit being computed is not the one the
+// refill overwrites.
 #pragma once
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 
@@ -56,6 +66,7 @@ struct StreamKParams {
     int64_t U;      // units = row_blocks * KC
     int32_t KC;     // units per row block
     int32_t whole;  // CTA ranges in whole row blocks (no row block shared by CTAs)
+    int32_t P;      // CTAs taking part (CTAs from P on have no work)
     Scratch scratch;
 };
 
@@ -114,7 +125,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
         store_y<B, F32OUT>(p.y, p.rows, row, tot);
         return;
     }
-    const int64_t U = p.U, P = gridDim.x;
+    const int64_t U = p.U, P = p.P;
     const int64_t c = blockIdx.x;
     const int64_t first = div64(((rb_lo + 1) * (P)) - 1, U);
     const int64_t last = div64(((rb_hi) * (P)) - 1, U);
@@ -198,94 +209,144 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
     finish_across_ctas<B, F32OUT>(p, cr, rb, tot, lane);
 }
 
+// Bytes of one warp's x ring (NBUF + 1 slots).
+template <class Pol, int B, int NBUF> constexpr int xring_bytes() { return (NBUF + 1) * Pol::template x_bytes<B>(); }
+
 template <class Pol, int B, int W, int NBUF> constexpr int streamk_smem_bytes()
 {
-    return 1024 + W * NBUF * Pol::template stage_bytes<B>() + W * (kGuardBytes + Pol::template xf_bytes<B>()) +
-           W * part_bytes<B>() + W * 4 + 16 + Pol::kSharedBytes;
+    return 1024 + W * NBUF * Pol::template stage_bytes<B>() + W * xring_bytes<Pol, B, NBUF>() +
+           W * (kGuardBytes + Pol::template xf_bytes<B>()) + W * part_bytes<B>() + W * 4 + 16 + Pol::kSharedBytes;
 }
 
-template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
-__global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_constant__ TensorMaps maps,
-                                                                const StreamKParams p)
+// Dynamic shared memory of a CTA: per-warp stage buffers (1024-aligned for
+// the 128-byte swizzle), per-warp x rings (128-aligned), per-warp fp32 x
+// windows, per-warp partial-sum slots, then the policy's CTA-wide region
+// (16-byte aligned).
+template <class Pol, int B, int W, int NBUF> struct SmemLayout {
+    uint8_t *stage0p; // this warp's first stage buffer
+    uint8_t *xring;   // this warp's first x slot
+    uint8_t *xfp;     // this warp's x window
+    float *part;      // partial-sum slots of all warps
+    uint8_t *pol;     // the policy's region
+    __device__ __forceinline__ SmemLayout(uint8_t *dsmem, int warp)
+    {
+        constexpr int SB = Pol::template stage_bytes<B>();
+        constexpr int XR = xring_bytes<Pol, B, NBUF>();
+        constexpr int XF = Pol::template xf_bytes<B>();
+        static_assert(SB % 1024 == 0 && XR % 128 == 0, "stage and x-slot alignment");
+        uint8_t *const sbase = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
+        stage0p = sbase + warp * NBUF * SB;
+        uint8_t *const xbase = sbase + W * NBUF * SB;
+        xring = xbase + warp * XR;
+        uint8_t *const fbase = xbase + W * XR;
+        xfp = fbase + warp * (kGuardBytes + XF) + kGuardBytes;
+        part = (float *)(fbase + W * (kGuardBytes + XF));
+        // pointer arithmetic only (no integer round trip), so that loads
+        // through `pol` stay shared-memory loads
+        uint8_t *const after = (uint8_t *)part + W * part_bytes<B>() + W * 4;
+        pol = after + ((16u - (smem_addr(after) & 15u)) & 15u);
+    }
+};
+
+// The CTA's unit range: whole row blocks or an even share of the units.
+__device__ __forceinline__ CtaRange cta_range(const StreamKParams &p, int W, int c)
+{
+    CtaRange cr;
+    if (c >= p.P) {
+        cr.cs = cr.ce = 0;
+        cr.nw = 0;
+        return cr;
+    }
+    if (p.whole) {
+        const int64_t nrb = div64(p.U, p.KC);
+        cr.cs = muldiv(nrb, c, p.P) * p.KC;
+        cr.ce = muldiv(nrb, c + 1, p.P) * p.KC;
+    } else {
+        cr.cs = muldiv(p.U, c, p.P);
+        cr.ce = muldiv(p.U, c + 1, p.P);
+    }
+    cr.nw = (int)((cr.ce - cr.cs) < W ? (cr.ce - cr.cs) : W);
+    return cr;
+}
+
+// A warp's contiguous share of its CTA's range.
+struct WarpWork {
+    int64_t ub, ue; // units [ub, ue)
+    int n;          // ue - ub
+    int32_t rb0;    // row block of unit ub
+    int32_t kc0;    // position of unit ub in its row block
+};
+
+__device__ __forceinline__ WarpWork warp_work(const CtaRange &cr, int32_t KC, int warp)
+{
+    WarpWork w;
+    w.ub = w.ue = 0;
+    if (warp < cr.nw) {
+        const int64_t n_cta = cr.ce - cr.cs;
+        w.ub = cr.cs + muldiv(n_cta, warp, cr.nw);
+        w.ue = cr.cs + muldiv(n_cta, warp + 1, cr.nw);
+    }
+    w.n = (int)(w.ue - w.ub);
+    w.rb0 = (int32_t)div64(w.ub, KC);
+    w.kc0 = (int32_t)(w.ub - (int64_t)w.rb0 * KC);
+    return w;
+}
+
+// Lane 0: arm the stages of the warp's first min(n, NBUF) units (all bytes
+// of the stage expected) and request their weights. `it` counts the units
+// the warp consumed before; unit it + i uses stage (it + i) % NBUF.
+template <class Pol, int B, int NBUF>
+__device__ __forceinline__ void issue_prologue_weights(const TensorMaps *maps, const WarpWork &w, int32_t KC,
+                                                       uint32_t it, uint32_t stage0, uint32_t bar0, uint64_t pol)
 {
     constexpr int SB = Pol::template stage_bytes<B>();
     constexpr uint32_t TX = Pol::template tx_bytes<B>();
-    constexpr int XF = Pol::template xf_bytes<B>();
-    __shared__ __align__(8) uint64_t full_bar[W * NBUF];
-    extern __shared__ __align__(1024) uint8_t dsmem[];
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    uint8_t *const sbase = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
-    uint8_t *const stage0p = sbase + warp * NBUF * SB;
-    uint8_t *const xfp = sbase + W * NBUF * SB + warp * (kGuardBytes + XF) + kGuardBytes;
-    float *const part = (float *)(sbase + W * NBUF * SB + W * (kGuardBytes + XF));
-    uint32_t *const cnt = (uint32_t *)((uint8_t *)part + W * part_bytes<B>());
-    // 16-byte aligned policy region (the tables are copied with 16-byte stores)
-    uint8_t *const pol_smem = (uint8_t *)(((uintptr_t)(cnt + W) + 15) & ~(uintptr_t)15);
-    const uint32_t stage0 = smem_addr(stage0p);
-    const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
-
-    CtaRange cr;
-    if (p.whole) {
-        const int64_t nrb = div64(p.U, p.KC);
-        cr.cs = muldiv(nrb, blockIdx.x, gridDim.x) * p.KC;
-        cr.ce = muldiv(nrb, blockIdx.x + 1, gridDim.x) * p.KC;
-    } else {
-        cr.cs = muldiv(p.U, blockIdx.x, gridDim.x);
-        cr.ce = muldiv(p.U, blockIdx.x + 1, gridDim.x);
-    }
-    cr.nw = (int)((cr.ce - cr.cs) < W ? (cr.ce - cr.cs) : W);
-
-    Pol::init_shared(pol_smem, threadIdx.x, W * 32);
-    if (lane == 0) {
-        for (int i = 0; i < NBUF; ++i)
-            mbar_init(bar0 + 8 * i, 1);
-        fence_mbar_init();
-    }
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&maps.w);
-        if (Pol::kHasMasks)
-            prefetch_tensormap(&maps.m);
-        prefetch_tensormap(&maps.x);
-    }
-    __syncthreads();
-
-    const bool active = warp < cr.nw;
-    const int64_t n_cta = cr.ce - cr.cs;
-    const int64_t ub = active ? cr.cs + muldiv(n_cta, warp, cr.nw) : 0;
-    const int64_t ue = active ? cr.cs + muldiv(n_cta, warp + 1, cr.nw) : 0;
-    const int n = (int)(ue - ub);
-    const int32_t KC = p.KC;
-    const int32_t rb0 = (int32_t)div64(ub, KC);
-    const int32_t kc0 = (int32_t)(ub - (int64_t)rb0 * KC);
-
-    // Weights do not depend on the previous kernel: start streaming them now.
-    const uint64_t pol = l2_policy_evict_first();
-    const int npre = n < NBUF ? n : NBUF;
-    if (lane == 0) {
-        int32_t rb = rb0, kc = kc0;
-        for (int i = 0; i < npre; ++i) {
-            mbar_arrive_expect_tx(bar0 + 8 * i, TX);
-            Pol::issue_weights(stage0 + i * SB, bar0 + 8 * i, kc, rb * kUnitRows, pol, maps);
-            if (++kc == KC) {
-                kc = 0;
-                ++rb;
-            }
+    const int npre = w.n < NBUF ? w.n : NBUF;
+    int32_t rb = w.rb0, kc = w.kc0;
+    for (int i = 0; i < npre; ++i) {
+        const uint32_t s = (it + i) % NBUF;
+        mbar_arrive_expect_tx(bar0 + 8 * s, TX);
+        Pol::issue_weights(stage0 + s * SB, bar0 + 8 * s, kc, rb * kUnitRows, pol, *maps);
+        if (++kc == KC) {
+            kc = 0;
+            ++rb;
         }
     }
-    // x may be the previous kernel's output.
-    pdl_wait_upstream();
-    if (lane == 0) {
-        int32_t kc = kc0;
-        for (int i = 0; i < npre; ++i) {
-            tma_load_2d(stage0 + i * SB + Pol::kXOffset, &maps.x, kc * Pol::kCols, 0, bar0 + 8 * i);
-            if (++kc == KC)
-                kc = 0;
-        }
-    }
-    pdl_launch_dependents();
+}
 
+// Lane 0: request the x slices of the same units; unit it + i uses x slot
+// (it + i) % (NBUF + 1) and completes on its stage's barrier.
+template <class Pol, int B, int NBUF>
+__device__ __forceinline__ void issue_prologue_x(const TensorMaps *maps, const WarpWork &w, int32_t KC, uint32_t it,
+                                                 uint32_t xr0, uint32_t bar0)
+{
+    constexpr int XB = Pol::template x_bytes<B>();
+    const int npre = w.n < NBUF ? w.n : NBUF;
+    int32_t kc = w.kc0;
+    for (int i = 0; i < npre; ++i) {
+        const uint32_t j = it + i;
+        tma_load_2d(xr0 + (j % (NBUF + 1)) * XB, &maps->x, kc * Pol::kCols, 0, bar0 + 8 * (j % NBUF));
+        if (++kc == KC)
+            kc = 0;
+    }
+}
+
+// Consume the warp's n units (their first min(n, NBUF) already requested):
+// for each, wait for its stage, copy its weights into registers, refill the
+// stage with the unit NBUF ahead, then do the arithmetic. A segment (the part
+// of a row block in this range) that is a whole row block is stored directly;
+// other segments leave their sum in the warp's partial slot (0: the range's
+// first row block, 1: its last).
+template <class Pol, int B, int W, int NBUF, bool F32OUT>
+__device__ __forceinline__ void consume_range(const TensorMaps *maps, const StreamKParams &p, const WarpWork &w,
+                                              uint32_t it, uint32_t stage0, const uint8_t *stage0p, uint32_t bar0,
+                                              uint32_t xr0, const uint8_t *xringp, uint8_t *xfp,
+                                              const uint8_t *pol_smem, float *part, int warp, int lane, uint64_t pol,
+                                              typename Pol::State &pst, bool &dead)
+{
+    constexpr int SB = Pol::template stage_bytes<B>();
+    constexpr int XB = Pol::template x_bytes<B>();
+    constexpr uint32_t TX = Pol::template tx_bytes<B>();
     float acc[4][B];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -293,35 +354,39 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
         for (int b = 0; b < B; ++b)
             acc[q][b] = 0.f;
 
-    int32_t rb = rb0, kc = kc0;   // unit being consumed
-    int32_t prb = rb0, pkc = kc0; // unit to prefetch next (i + NBUF)
-    for (int i = 0; i < npre; ++i) {
+    const int32_t KC = p.KC;
+    const int n = w.n;
+    int32_t rb = w.rb0, kc = w.kc0;   // unit being consumed
+    int32_t prb = w.rb0, pkc = w.kc0; // unit to request next (i + NBUF)
+    for (int i = 0; i < (n < NBUF ? n : NBUF); ++i) {
         if (++pkc == KC) {
             pkc = 0;
             ++prb;
         }
     }
-    int32_t seg_kc0 = kc0; // first unit of the current segment, as kc
-    bool dead = false;
-    typename Pol::State pst = Pol::initial_state();
+    int32_t seg_kc0 = w.kc0; // first unit of the current segment, as kc
     for (int i = 0; i < n; ++i) {
-        const int s = i % NBUF;
+        const uint32_t j = it + (uint32_t)i;
+        const int s = (int)(j % NBUF);
         const uint32_t st = stage0 + s * SB, bar = bar0 + 8 * s;
-        mbar_wait_bounded(bar, (uint32_t)((i / NBUF) & 1), p.scratch.status, dead);
-        Pol::template consume<B>(stage0p + s * SB, xfp, pol_smem, pst, lane, acc);
-        __syncwarp();
+        mbar_wait_bounded(bar, (j / NBUF) & 1u, p.scratch.status, dead);
+        typename Pol::template Regs<B> r;
+        Pol::template load<B>(stage0p + s * SB, lane, r);
+        __syncwarp(); // every lane's reads of the stage are done
         if (i + NBUF < n) {
-            if (lane == 0) {
+            if (lane == 0 && !dead) {
+                const uint32_t jn = j + NBUF;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, TX);
-                Pol::issue_weights(st, bar, pkc, prb * kUnitRows, pol, maps);
-                tma_load_2d(st + Pol::kXOffset, &maps.x, pkc * Pol::kCols, 0, bar);
+                Pol::issue_weights(st, bar, pkc, prb * kUnitRows, pol, *maps);
+                tma_load_2d(xr0 + (jn % (NBUF + 1)) * XB, &maps->x, pkc * Pol::kCols, 0, bar);
             }
             if (++pkc == KC) {
                 pkc = 0;
                 ++prb;
             }
         }
+        Pol::template compute<B>(r, xringp + (j % (NBUF + 1)) * XB, xfp, pol_smem, pst, lane, acc);
         if (kc + 1 == KC || i == n - 1) { // end of a segment (row block or range)
             float tot[B];
 #pragma unroll
@@ -334,7 +399,7 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
             if (seg_kc0 == 0 && kc + 1 == KC) {
                 store_y<B, F32OUT>(p.y, p.rows, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
             } else {
-                float *mine = part + ((warp * 2 + (rb == rb0 ? 0 : 1)) * B) * 32 + lane;
+                float *mine = part + ((warp * 2 + (rb == w.rb0 ? 0 : 1)) * B) * 32 + lane;
 #pragma unroll
                 for (int b = 0; b < B; ++b)
                     mine[b * 32] = tot[b];
@@ -346,13 +411,198 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
             ++rb;
         }
     }
+}
+
+// After the CTA barrier that follows consume_range: finish the warp's first
+// and last row block (the only segments that can be partial).
+template <int B, bool F32OUT>
+__device__ __forceinline__ void finish_warp(const StreamKParams &p, const CtaRange &cr, const float *part,
+                                            const WarpWork &w, int lane)
+{
+    if (w.n <= 0)
+        return;
+    const int64_t KC = p.KC;
+    const int64_t rbf = w.rb0, rbl = div64(w.ue - 1, KC);
+    finish_in_cta<B, F32OUT>(p, cr, part, rbf, w.ub, rbf == rbl ? w.ue : (rbf + 1) * KC, lane);
+    if (rbl != rbf)
+        finish_in_cta<B, F32OUT>(p, cr, part, rbl, rbl * KC, w.ue, lane);
+}
+
+template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
+__global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_constant__ TensorMaps maps,
+                                                                const StreamKParams p)
+{
+    __shared__ __align__(8) uint64_t full_bar[W * NBUF];
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const SmemLayout<Pol, B, W, NBUF> sm(dsmem, warp);
+    const uint32_t stage0 = smem_addr(sm.stage0p);
+    const uint32_t xr0 = smem_addr(sm.xring);
+    const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
+    const CtaRange cr = cta_range(p, W, blockIdx.x);
+    const WarpWork w = warp_work(cr, p.KC, warp);
+
+    // Each warp's barriers are its own (initialised, armed and waited on by
+    // the warp): the weights of its first stages, which do not depend on the
+    // previous kernel, are requested before anything else.
+    const uint64_t pol = l2_policy_evict_first();
+    if (lane == 0) {
+        for (int i = 0; i < NBUF; ++i)
+            mbar_init(bar0 + 8 * i, 1);
+        fence_mbar_init();
+        issue_prologue_weights<Pol, B, NBUF>(&maps, w, p.KC, 0, stage0, bar0, pol);
+    }
+    Pol::init_shared(sm.pol, threadIdx.x, W * 32); // overlaps the first weight copies
+    __syncthreads();
+    // x may be the previous kernel's output.
+    pdl_wait_upstream();
+    if (lane == 0)
+        issue_prologue_x<Pol, B, NBUF>(&maps, w, p.KC, 0, xr0, bar0);
+    pdl_launch_dependents();
+
+    bool dead = false;
+    typename Pol::State pst = Pol::initial_state();
+    consume_range<Pol, B, W, NBUF, F32OUT>(&maps, p, w, 0, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp, sm.pol,
+                                           sm.part, warp,
+                                           lane, pol, pst, dead);
     __syncthreads(); // every partial of this CTA is in shared memory
-    if (n > 0) {
-        // the first and the last segment are the only ones that can be partial
-        const int64_t rbf = rb0, rbl = div64(ue - 1, KC);
-        finish_in_cta<B, F32OUT>(p, cr, part, rbf, ub, rbf == rbl ? ue : (rbf + 1) * (int64_t)KC, lane);
-        if (rbl != rbf)
-            finish_in_cta<B, F32OUT>(p, cr, part, rbl, rbl * (int64_t)KC, ue, lane);
+    finish_warp<B, F32OUT>(p, cr, sm.part, w, lane);
+}
+
+// ---------------------------------------------------------------------------
+// The whole decode-token stack as one persistent launch
+// ---------------------------------------------------------------------------
+
+// One linear of a stack, as the persistent kernel reads it from global memory.
+struct StackOp { // aligned as CUtensorMap requires
+    TensorMaps maps;
+    void *y;
+    int64_t rows;
+    int64_t U;
+    int32_t KC;
+    int32_t whole;
+    int32_t P;
+    int32_t reserved;
+};
+
+__device__ __forceinline__ StreamKParams op_params(const StackOp *op, const Scratch &scratch)
+{
+    StreamKParams p;
+    p.y = op->y;
+    p.rows = op->rows;
+    p.U = op->U;
+    p.KC = op->KC;
+    p.whole = op->whole;
+    p.P = op->P;
+    p.scratch = scratch;
+    return p;
+}
+
+// Barrier over every CTA of a cooperative launch, by sense reversal on one
+// counter: CTA 0 adds 2^31 - (n - 1) and every other CTA adds 1, so the top
+// bit flips exactly when the n-th CTA arrives and the low 31 bits return to
+// where they were. Whatever the order of arrivals, each barrier adds 2^31 in
+// total, so the counter is ready for the next launch as long as every CTA
+// arrives at every barrier -- which each does, waits being bounded. A wait
+// that runs out records NM_ERR_TIMEOUT and marks the CTA dead: it stops
+// requesting data and its later waits return at once.
+__device__ __forceinline__ void grid_barrier(uint32_t *ctr, uint32_t *status, bool &dead)
+{
+    __shared__ uint32_t s_timed_out;
+    __syncthreads(); // every write of this CTA before the barrier is done
+    if (threadIdx.x == 0) {
+        const uint32_t add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+        __threadfence();
+        const uint32_t old = atomicAdd(ctr, add);
+        uint32_t to = 0;
+        if (!dead) {
+            const uint64_t t0 = globaltimer_ns();
+            while (((ld_acquire_gpu(ctr) ^ old) & 0x80000000u) == 0u) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(status, 1u << NM_ERR_TIMEOUT);
+                    to = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+        s_timed_out = to;
+    }
+    __syncthreads();
+    if (s_timed_out)
+        dead = true;
+}
+
+// Runs ops[0..n_ops) in order. Each CTA takes the same place in every op's
+// split as the single-launch kernel would give it; between two ops a grid
+// barrier stands in for the kernel boundary (x of op l+1 is read only after
+// every CTA has stored its part of op l). Before arriving there, each warp
+// requests the weights of its first stages of op l+1, which keeps HBM busy
+// across the barrier.
+template <class Pol, int B, int W, int NBUF, int MINB>
+__global__ void __launch_bounds__(W * 32, MINB)
+    stack_kernel(const StackOp *__restrict__ ops, const int n_ops, uint32_t *const gbar, const Scratch scratch)
+{
+    __shared__ __align__(8) uint64_t full_bar[W * NBUF];
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const SmemLayout<Pol, B, W, NBUF> sm(dsmem, warp);
+    const uint32_t stage0 = smem_addr(sm.stage0p);
+    const uint32_t xr0 = smem_addr(sm.xring);
+    const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
+
+    const uint64_t pol = l2_policy_evict_first();
+    typename Pol::State pst = Pol::initial_state();
+    bool dead = false;
+    uint32_t it = 0; // units this warp has consumed so far, over all ops
+    StreamKParams p = op_params(&ops[0], scratch);
+    CtaRange cr = cta_range(p, W, blockIdx.x);
+    WarpWork w = warp_work(cr, p.KC, warp);
+    if (lane == 0) {
+        for (int i = 0; i < NBUF; ++i)
+            mbar_init(bar0 + 8 * i, 1);
+        fence_mbar_init();
+        issue_prologue_weights<Pol, B, NBUF>(&ops[0].maps, w, p.KC, it, stage0, bar0, pol);
+    }
+    Pol::init_shared(sm.pol, threadIdx.x, W * 32); // overlaps the first weight copies
+    __syncthreads();
+    for (int l = 0;; ++l) {
+        const TensorMaps *maps = &ops[l].maps;
+        const bool more = l + 1 < n_ops;
+        const StackOp *next = &ops[more ? l + 1 : l];
+        if (threadIdx.x == 0 && more) {
+            prefetch_tensormap(&next->maps.w);
+            if (Pol::kHasMasks)
+                prefetch_tensormap(&next->maps.m);
+            prefetch_tensormap(&next->maps.x);
+        }
+        if (lane == 0 && !dead) {
+            fence_proxy_async_global(); // x may hold other CTAs' stores from before the barrier
+            issue_prologue_x<Pol, B, NBUF>(maps, w, p.KC, it, xr0, bar0);
+        }
+        consume_range<Pol, B, W, NBUF, false>(maps, p, w, it, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp, sm.pol,
+                                              sm.part,
+                                              warp, lane, pol, pst, dead);
+        it += (uint32_t)w.n;
+        const StreamKParams pn = op_params(next, scratch);
+        const CtaRange crn = cta_range(pn, W, blockIdx.x);
+        const WarpWork wn = warp_work(crn, pn.KC, warp);
+        if (more && lane == 0 && !dead) {
+            fence_proxy_async_smem(); // the stages were read by this warp's loads
+            issue_prologue_weights<Pol, B, NBUF>(&next->maps, wn, pn.KC, it, stage0, bar0, pol);
+        }
+        __syncthreads(); // every partial of this CTA is in shared memory
+        finish_warp<B, false>(p, cr, sm.part, w, lane);
+        if (!more)
+            break;
+        grid_barrier(gbar, scratch.status, dead);
+        p = pn;
+        cr = crn;
+        w = wn;
     }
 }
 
@@ -385,9 +635,8 @@ struct Split {
 // that keeps the CTAs within ~15% of even work and gives no warp more than
 // about three units beyond an even split over all slots (the fix-up costs
 // about that much); otherwise split units evenly (stream-K) over all slots.
-inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
+inline Split choose_split_slots(int64_t nrb, int64_t KC, int W, int64_t slots)
 {
-    const int64_t slots = (int64_t)num_sms * minb;
     const int64_t U = nrb * KC;
     Split sp;
     sp.ctas = std::min<int64_t>(nrb, slots);
@@ -400,6 +649,11 @@ inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
         sp.ctas = std::max<int64_t>(1, std::min<int64_t>(slots, U / kMinUnitsPerCta));
     sp.ctas = std::min<int64_t>(sp.ctas, kMaxCtas);
     return sp;
+}
+
+inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
+{
+    return choose_split_slots(nrb, KC, W, (int64_t)num_sms * minb);
 }
 
 // Launch the stream-K kernel for a problem of `rows` rows and KC units per row
@@ -429,6 +683,7 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows;
     const Split sp = choose_split(nrb, KC, W, MINB, ctx.num_sms);
     p.whole = sp.whole ? 1 : 0;
+    p.P = (int32_t)sp.ctas;
     const int64_t ctas = sp.ctas;
 
     cudaLaunchConfig_t cfg = {};
@@ -444,6 +699,80 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     if (cudaLaunchKernelEx(&cfg, kern, maps, p) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_OK;
+}
+
+// The persistent stack kernel of one configuration: grid size (every CTA
+// resident, as a cooperative launch requires), the split of each op over that
+// grid, and the launch.
+template <class Pol, int B, int W, int NBUF, int MINB> struct StackLauncher {
+    static constexpr int kSmem = streamk_smem_bytes<Pol, B, W, NBUF>();
+    static_assert(MINB * (kSmem + 1024) <= 232448, "MINB CTAs must fit one SM's shared memory");
+
+    // CTAs of the launch: MINB per SM, fewer if fewer fit.
+    static nm_status grid(int num_sms, int *ctas)
+    {
+        auto kern = stack_kernel<Pol, B, W, NBUF, MINB>;
+        static std::once_flag once;
+        static cudaError_t attr_err = cudaSuccess;
+        std::call_once(once, [&] {
+            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        });
+        if (attr_err != cudaSuccess)
+            return NM_ERR_CUDA;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, W * 32, kSmem) != cudaSuccess || occ < 1)
+            return NM_ERR_CUDA;
+        *ctas = std::min(std::min(occ, MINB) * num_sms, kMaxCtas);
+        return NM_OK;
+    }
+
+    // Fill op's split fields for a grid of `ctas` CTAs (maps are set by the caller).
+    static void split(StackOp *op, void *y, int64_t rows, int64_t KC, int ctas)
+    {
+        const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows;
+        const Split sp = choose_split_slots(nrb, KC, W, ctas);
+        op->y = y;
+        op->rows = rows;
+        op->U = nrb * KC;
+        op->KC = (int32_t)KC;
+        op->whole = sp.whole ? 1 : 0;
+        op->P = (int32_t)std::min<int64_t>(sp.ctas, ctas);
+        op->reserved = 0;
+    }
+
+    static nm_status launch(const StackOp *ops, int n_ops, uint32_t *gbar, int ctas, const LaunchCtx &ctx)
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3(W * 32);
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = ctx.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative; // the grid barrier needs every CTA resident
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, stack_kernel<Pol, B, W, NBUF, MINB>, ops, n_ops, gbar, ctx.scratch) !=
+            cudaSuccess)
+            return NM_ERR_CUDA;
+        return NM_OK;
+    }
+};
+
+// Calls f(std::integral_constant<int, batch>) for batch 1..8.
+template <class F> nm_status with_batch(int batch, F &&f)
+{
+    switch (batch) {
+    case 1: return f(std::integral_constant<int, 1>{});
+    case 2: return f(std::integral_constant<int, 2>{});
+    case 3: return f(std::integral_constant<int, 3>{});
+    case 4: return f(std::integral_constant<int, 4>{});
+    case 5: return f(std::integral_constant<int, 5>{});
+    case 6: return f(std::integral_constant<int, 6>{});
+    case 7: return f(std::integral_constant<int, 7>{});
+    case 8: return f(std::integral_constant<int, 8>{});
+    default: return NM_ERR_UNSUPPORTED;
+    }
 }
 
 // x slice of one unit, bf16 [B][cols] in the stage -> fp32 [cols][BP] in the warp's buffer.

@@ -119,6 +119,17 @@ def test_argument_validation_before_any_cuda_call(nm):
     ops[1].K = 40
     assert L.nm_spmv_stack(ops, 2, 1, None) == nm.NM_ERR_SHAPE
     assert L.nm_spmv_stack(None, 1, 1, None) == nm.NM_ERR_INVALID_ARG
+    # a plan is validated before any device work as well
+    h = ctypes.c_void_p()
+    assert L.nm_stack_plan_create(ops, 2, 1, 0, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_stack_plan_create(ops, -1, 1, 0, ctypes.byref(h)) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_stack_plan_create(ops, 2, 1, 0, ctypes.byref(h)) == nm.NM_ERR_SHAPE
+    assert L.nm_stack_plan_create(ops, 1, 9, 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_stack_plan_create(None, 0, 0, 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_stack_plan_create(ops, 1, 1, 4, ctypes.byref(h)) == nm.NM_ERR_INVALID_ARG  # unknown flag
+    assert h.value is None  # not set on error
+    assert L.nm_stack_plan_run(None, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_stack_plan_destroy(None) == nm.NM_OK
 
 
 def test_no_fallback_when_library_missing(monkeypatch):

@@ -375,5 +375,118 @@ def test_stack_in_cuda_graph(nm):
         assert torch.equal(op["y"], nm.spmv(m, v, x))
 
 
+# --- stack plans: the whole stack as one persistent launch ------------------------------------
+
+def check_bf16(ybf: np.ndarray, y64: np.ndarray, S: np.ndarray, what: str):
+    """bf16 output alone: within one ulp of y64 (plus 1e-4*S where |y64| < 1e-4*S)."""
+    yb = bits_to_f32(ybf).astype(np.float64)
+    err = np.abs(yb - y64)
+    bound = bf16_ulp(y64) + np.where(np.abs(y64) >= TOL * S, 0.0, TOL * S)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{what}: {np.argwhere(bad)[:5]} err {err[bad][:5]} bound {bound[bad][:5]}"
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("dense", [False, True])
+@pytest.mark.parametrize("persistent", [False, True])
+def test_plan_matches_oracle(nm, batch, dense, persistent):
+    ops_s, ops_d, refs = _stack_inputs(nm, batch)
+    ops = ops_d if dense else ops_s
+    for op in ops:
+        op["y"].fill_(float("nan"))
+    plan = nm.StackPlan(ops, batch, dense=dense, persistent=persistent)
+    plan.run()
+    torch.cuda.synchronize()
+    for i, (op, (_, _, x, W)) in enumerate(zip(ops, refs)):
+        y64, S = oracle.spmv_f64(to_bits(W.cpu()), to_bits(x.cpu()))
+        check_bf16(to_bits(op["y"]), y64, S, f"plan op {i} {'dense' if dense else 'sparse'} b{batch}")
+    plan.close()
+    assert nm.device_status() == nm.NM_OK
+
+
+# A chain in which op i+1 reads op i's output: an op that read its x before the
+# previous op had stored all of it would see NaN (outputs start as NaN) or a
+# stale value, and miss the oracle computed on what it actually read.
+@pytest.mark.parametrize("batch", [1, 3])
+@pytest.mark.parametrize("persistent", [False, True])
+def test_plan_chained_dependency(nm, batch, persistent):
+    shapes = [(1024, 4096), (2048, 1024), (512, 2048), (4096, 512), (896, 4096), (4096, 896),
+              (128, 4096), (6144, 128), (4096, 6144), (4096, 4096), (32, 4096), (4096, 32)]
+    shapes = [(r, k) for r, k in shapes if k % 128 == 0]
+    for (r0, _), (_, k1) in zip(shapes, shapes[1:]):
+        assert r0 == k1
+    x0 = synth.activations(batch, shapes[0][1], seed=5).cuda()
+    ops, Ws, x = [], [], x0
+    for i, (rows, K) in enumerate(shapes):
+        W = synth.nm_structured(rows, K, 2, 4, seed=50 + i)
+        # keep the chain's values O(1): scale by 1/sqrt(K/2 * 0.02^2)
+        W = (W.float() * (1.0 / (0.02 * (K / 2) ** 0.5))).to(torch.bfloat16)
+        m, v = nm.pack(W.cuda(), 2, 4)
+        y = torch.full((batch, rows), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ops.append(dict(masks=m, values=v, x=x, y=y, rows=rows, K=K))
+        Ws.append(W)
+        x = y
+    plan = nm.StackPlan(ops, batch, persistent=persistent)
+    for rep in range(3):
+        for op in ops:
+            op["y"].fill_(float("nan"))
+        plan.run()
+        torch.cuda.synchronize()
+        for i, (op, W) in enumerate(zip(ops, Ws)):
+            xin = to_bits(op["x"].cpu())  # what op i actually read: op i-1's output
+            assert not np.isnan(bits_to_f32(xin)).any(), f"op {i}: input still NaN"
+            y64, S = oracle.spmv_f64(to_bits(W), xin)
+            check_bf16(to_bits(op["y"]), y64, S, f"chain op {i} rep {rep}")
+    plan.close()
+    assert nm.device_status() == nm.NM_OK
+
+
+@pytest.mark.parametrize("persistent", [False, True])
+def test_plan_repeats_and_graph_replay_bit_exact(nm, persistent):
+    ops_s, _, _ = _stack_inputs(nm, 1)
+    plan = nm.StackPlan(ops_s, 1, persistent=persistent)
+    plan.run()
+    torch.cuda.synchronize()
+    first = [op["y"].clone() for op in ops_s]
+    for _ in range(20):
+        plan.run()
+    torch.cuda.synchronize()
+    for op, f in zip(ops_s, first):
+        assert torch.equal(op["y"], f)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            plan.run()
+    torch.cuda.current_stream().wait_stream(s)
+    for op in ops_s:
+        op["y"].zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for op, f in zip(ops_s, first):
+        assert torch.equal(op["y"], f)
+    plan.close()
+    assert nm.device_status() == nm.NM_OK
+
+
+def test_plan_falls_back_to_chained_launches(nm):
+    # K = 96 is off the TMA path: the plan runs the ops as nm_spmv_stack would
+    ops_s, _, refs = _stack_inputs(nm, 2, layers=1)
+    W = synth.nm_structured(40, 96, 2, 4, seed=3).cuda()
+    m, v = nm.pack(W, 2, 4)
+    x = synth.activations(2, 96, seed=4).cuda()
+    ops = ops_s + [dict(masks=m, values=v, x=x, y=torch.empty(2, 40, dtype=torch.bfloat16, device="cuda"),
+                        rows=40, K=96)]
+    refs = refs + [(m, v, x, W)]
+    plan = nm.StackPlan(ops, 2, persistent=True)
+    plan.run()
+    torch.cuda.synchronize()
+    for op, (m, v, x, _) in zip(ops, refs):
+        assert torch.equal(op["y"], nm.spmv(m, v, x))
+    plan.close()
+
+
 def test_no_bounded_wait_ran_out(nm):
     assert nm.device_status() == nm.NM_OK
