@@ -239,7 +239,9 @@ nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const 
 /*
  * nm_device_status -- waits for `stream`, then returns and clears the status
  * word of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
- * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed).
+ * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed). After
+ * a timeout it also clears the scratch's stream-K counters (outputs of the
+ * calls that ran meanwhile are unspecified); call it before reusing the device.
  */
 nm_status nm_device_status(void *stream);
 

@@ -400,7 +400,14 @@ nm_status nm_device_status(void *stream)
         cudaMemsetAsync(ctx.scratch.status, 0, sizeof word, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
-    return (word & (1u << NM_ERR_TIMEOUT)) ? NM_ERR_TIMEOUT : NM_OK;
+    if (!(word & (1u << NM_ERR_TIMEOUT)))
+        return NM_OK;
+    // A kernel that gave up may have left the stream-K counters mid-count:
+    // clear them, so that later calls start from a clean state.
+    if (cudaMemsetAsync(ctx.scratch.counters, 0, kScratchCounterBytes, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    return NM_ERR_TIMEOUT;
 }
 
 } // extern "C"
