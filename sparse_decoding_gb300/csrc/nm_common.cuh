@@ -61,6 +61,22 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f)
     return r;
 }
 
+// acc + w * x, where w and x are bf16 values held in the low (H = 0) or high
+// (H = 1) half of 32-bit registers. The product of two bf16 values is exact in
+// fp32, so this equals fmaf(float(w), float(x), acc) bit for bit; the
+// mixed-precision form reads the halves directly, with no conversion.
+template <int WH, int XH>
+__device__ __forceinline__ float fma_bf16(uint32_t w, uint32_t x, float acc)
+{
+    asm("{\n\t.reg .b16 w0, w1, x0, x1;\n\t"
+        "mov.b32 {w0, w1}, %1;\n\t"
+        "mov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, w%3, x%4, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x), "n"(WH), "n"(XH));
+    return acc;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory access by 32-bit shared address
 // ---------------------------------------------------------------------------

@@ -164,16 +164,17 @@ __device__ __forceinline__ bool walk_unit_b1_lut(const uint32_t (&m)[4], const u
         return false;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float xr = bf16_to_f32(*(const uint16_t *)(sx + (32 * q + lane) * 2));
+        // x stays bf16 (low half); one mixed-precision FMA per product
+        const uint32_t xr = *(const uint16_t *)(sx + (32 * q + lane) * 2);
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const uint32_t e = ent[q][b];
             const uint32_t p0 = v[q][2 * b], p1 = v[q][2 * b + 1];
-            a0 = fmaf(bf16lo_to_f32(p0), __shfl_sync(0xFFFFFFFFu, xr, (int)e), a0);
-            a1 = fmaf(bf16hi_to_f32(p0), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 8)), a1);
-            a0 = fmaf(bf16lo_to_f32(p1), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 16)), a0);
-            a1 = fmaf(bf16hi_to_f32(p1), __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 24)), a1);
+            a0 = fma_bf16<0, 0>(p0, __shfl_sync(0xFFFFFFFFu, xr, (int)e), a0);
+            a1 = fma_bf16<1, 0>(p0, __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 8)), a1);
+            a0 = fma_bf16<0, 0>(p1, __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 16)), a0);
+            a1 = fma_bf16<1, 0>(p1, __shfl_sync(0xFFFFFFFFu, xr, (int)(e >> 24)), a1);
         }
         acc[q][0] += a0 + a1;
     }

@@ -161,6 +161,51 @@ def test_spmv_llama8b_linears(nm, name, N, M):
     check_close(y32, ybf, y64, S, f"{name} {N}:{M}")
 
 
+# The other model shapes at full size (Qwen3-14B/32B with 4:8 and 8:16;
+# Llama-3.3-70B with 2:4 and 16:32): W is drawn on the GPU by the seeded
+# generator, packed and multiplied there; the oracle recomputes a sample of
+# rows (the first and last row block and 32 scattered rows) from the same
+# generator's rows copied back.
+MODEL_CASES = [("qwen3-14b", (4, 8)), ("qwen3-14b", (8, 16)), ("qwen3-32b", (4, 8)), ("qwen3-32b", (8, 16)),
+               ("llama3.3-70b", (2, 4)), ("llama3.3-70b", (16, 32))]
+
+
+def sampled_rows(rows: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    idx = np.concatenate([np.arange(min(32, rows)), np.arange(max(0, rows - 32), rows),
+                          rng.integers(0, rows, 32)])
+    return np.unique(idx)
+
+
+def check_sampled(nm, rows, K, N, M, batch, seed, what):
+    W = synth.nm_structured(rows, K, N, M, seed=seed, device="cuda")
+    m, v = nm.pack(W, N, M)
+    x = synth.activations(batch, K, seed=seed + 1, device="cuda")
+    y32 = nm.spmv(m, v, x, f32=True)
+    ybf = nm.spmv(m, v, x)
+    torch.cuda.synchronize()
+    idx = sampled_rows(rows, seed)
+    Wp = to_bits(W[torch.from_numpy(idx).cuda()].cpu())
+    y64, S = oracle.spmv_f64(Wp, to_bits(x.cpu()))
+    check_close(y32.cpu().numpy()[:, idx], to_bits(ybf)[:, idx], y64, S, what)
+    del W, m, v
+
+
+@pytest.mark.parametrize("model,pattern", MODEL_CASES)
+@pytest.mark.parametrize("name", ["qkv", "o", "gate_up", "down"])
+def test_spmv_model_linears_sampled(nm, model, pattern, name):
+    rows, K = synth.MODELS[model][name]
+    N, M = pattern
+    check_sampled(nm, rows, K, N, M, 1, seed=rows % 1000 + K % 997, what=f"{model} {name} {N}:{M}")
+
+
+@pytest.mark.parametrize("batch", [2, 4, 8])
+@pytest.mark.parametrize("name", ["o", "down"])
+def test_spmv_70b_batch_sweep_sampled(nm, batch, name):
+    rows, K = synth.LLAMA33_70B[name]
+    check_sampled(nm, rows, K, 2, 4, batch, seed=31 + batch, what=f"70b {name} b{batch}")
+
+
 @pytest.mark.parametrize("N,M", synth.PATTERNS)
 def test_spmv_exact_dyadic(nm, N, M):
     """Dyadic weights, small-integer x: fp32 is exact in any summation order."""
