@@ -67,8 +67,18 @@ struct StreamKParams {
     int32_t KC;     // units per row block
     int32_t whole;  // CTA ranges in whole row blocks (no row block shared by CTAs)
     int32_t P;      // CTAs taking part (CTAs from P on have no work)
+    int32_t shared_queue; // warps take the CTA's units from a shared counter (see consume_queue)
+    uint32_t kc_inv;      // ceil(2^32 / KC): n / KC = umulhi(n, kc_inv) for the small n used
     Scratch scratch;
 };
+
+// Units a CTA of W warps may take from its shared queue (batch 1): one fp32
+// partial per row and unit is kept in shared memory until the CTA's end.
+template <int W> constexpr int queue_cap() { return W >= 16 ? 128 : 96; }
+template <class Pol, int B, int W, int NBUF> constexpr int queue_bytes()
+{
+    return B == 1 ? 16 + W * NBUF * 4 + queue_cap<W>() * 32 * 4 : 0;
+}
 
 template <int B, bool F32OUT>
 __device__ __forceinline__ void store_y(void *y, int64_t rows, int64_t row, const float (&v)[B])
@@ -215,7 +225,8 @@ template <class Pol, int B, int NBUF> constexpr int xring_bytes() { return (NBUF
 template <class Pol, int B, int W, int NBUF> constexpr int streamk_smem_bytes()
 {
     return 1024 + W * NBUF * Pol::template stage_bytes<B>() + W * xring_bytes<Pol, B, NBUF>() +
-           W * (kGuardBytes + Pol::template xf_bytes<B>()) + W * part_bytes<B>() + W * 4 + 16 + Pol::kSharedBytes;
+           W * (kGuardBytes + Pol::template xf_bytes<B>()) + W * part_bytes<B>() + W * 4 + 16 + Pol::kSharedBytes +
+           queue_bytes<Pol, B, W, NBUF>();
 }
 
 // Dynamic shared memory of a CTA: per-warp stage buffers (1024-aligned for
@@ -228,6 +239,7 @@ template <class Pol, int B, int W, int NBUF> struct SmemLayout {
     uint8_t *xfp;     // this warp's x window
     float *part;      // partial-sum slots of all warps
     uint8_t *pol;     // the policy's region
+    uint8_t *queue;   // the shared queue: counter, per-stage unit numbers, per-unit partials
     __device__ __forceinline__ SmemLayout(uint8_t *dsmem, int warp)
     {
         constexpr int SB = Pol::template stage_bytes<B>();
@@ -245,6 +257,7 @@ template <class Pol, int B, int W, int NBUF> struct SmemLayout {
         // through `pol` stay shared-memory loads
         uint8_t *const after = (uint8_t *)part + W * part_bytes<B>() + W * 4;
         pol = after + ((16u - (smem_addr(after) & 15u)) & 15u);
+        queue = pol + Pol::kSharedBytes; // 16-byte aligned: kSharedBytes is a multiple of 16
     }
 };
 
@@ -428,6 +441,161 @@ __device__ __forceinline__ void finish_warp(const StreamKParams &p, const CtaRan
         finish_in_cta<B, F32OUT>(p, cr, part, rbl, rbl * KC, w.ue, lane);
 }
 
+// Batch 1, a CTA range of at most queue_cap<W>() units: the warps take the
+// CTA's units from a shared counter instead of fixed sub-ranges, so that a
+// warp whose data comes late does fewer units and the CTA's warps finish
+// together. Warp w's first NBUF units are units w*NBUF .. w*NBUF+NBUF-1 (set
+// before the CTA barrier, with no counter); the counter starts after them.
+// Each unit's sum goes to its own slot; after the CTA barrier every row block
+// is added in unit order (queue_finish), so the result does not depend on
+// which warp took which unit. The unit held by a stage is recorded next to
+// it by lane 0 before the stage's copies are requested.
+struct QueueView {
+    uint32_t *claim;      // next unit to hand out
+    uint32_t *stage_unit; // [W][NBUF]
+    float *upart;         // [cap][32]
+};
+
+template <class Pol, int B, int W, int NBUF>
+__device__ __forceinline__ QueueView queue_view(uint8_t *q)
+{
+    QueueView v;
+    v.claim = (uint32_t *)q;
+    v.stage_unit = (uint32_t *)(q + 16);
+    v.upart = (float *)(q + 16 + W * NBUF * 4);
+    return v;
+}
+
+// Row block and position of unit u of the CTA range starting at unit cs.
+__device__ __forceinline__ void queue_unit_coords(const StreamKParams &p, int64_t cs, uint32_t u, int32_t &rb,
+                                                  int32_t &kc)
+{
+    const int32_t rb_cs = (int32_t)div64(cs, p.KC);
+    const uint32_t k = (uint32_t)(cs - (int64_t)rb_cs * p.KC) + u; // < KC + cap
+    const uint32_t q = __umulhi(k, p.kc_inv);
+    rb = rb_cs + (int32_t)q;
+    kc = (int32_t)(k - q * (uint32_t)p.KC);
+}
+
+// Lane 0: the first units of this warp, requested before the CTA barrier.
+template <class Pol, int B, int NBUF>
+__device__ __forceinline__ int queue_prologue(const TensorMaps *maps, const StreamKParams &p, const CtaRange &cr,
+                                              QueueView qv, int warp, uint32_t stage0, uint32_t bar0, uint64_t pol)
+{
+    constexpr int SB = Pol::template stage_bytes<B>();
+    constexpr uint32_t TX = Pol::template tx_bytes<B>();
+    const uint32_t n = (uint32_t)(cr.ce - cr.cs);
+    int npre = 0;
+    for (int i = 0; i < NBUF; ++i) {
+        const uint32_t u = (uint32_t)(warp * NBUF + i);
+        if (u >= n)
+            break;
+        int32_t rb, kc;
+        queue_unit_coords(p, cr.cs, u, rb, kc);
+        qv.stage_unit[warp * NBUF + i] = u;
+        mbar_arrive_expect_tx(bar0 + 8 * i, TX);
+        Pol::issue_weights(stage0 + i * SB, bar0 + 8 * i, kc, rb * kUnitRows, pol, *maps);
+        ++npre;
+    }
+    return npre;
+}
+
+// Lane 0: x of the prologue's units.
+template <class Pol, int B, int NBUF>
+__device__ __forceinline__ void queue_prologue_x(const TensorMaps *maps, const StreamKParams &p, const CtaRange &cr,
+                                                 QueueView qv, int warp, int npre, uint32_t xr0, uint32_t bar0)
+{
+    constexpr int XB = Pol::template x_bytes<B>();
+    for (int i = 0; i < npre; ++i) {
+        int32_t rb, kc;
+        queue_unit_coords(p, cr.cs, qv.stage_unit[warp * NBUF + i], rb, kc);
+        tma_load_2d(xr0 + i * XB, &maps->x, kc * Pol::kCols, 0, bar0 + 8 * i);
+    }
+}
+
+template <class Pol, int B, int W, int NBUF>
+__device__ __forceinline__ void consume_queue(const TensorMaps *maps, const StreamKParams &p, const CtaRange &cr,
+                                              QueueView qv, int npre, uint32_t stage0, const uint8_t *stage0p,
+                                              uint32_t bar0, uint32_t xr0, const uint8_t *xringp, uint8_t *xfp,
+                                              const uint8_t *pol_smem, int warp, int lane, uint64_t pol,
+                                              typename Pol::State &pst, bool &dead)
+{
+    constexpr int SB = Pol::template stage_bytes<B>();
+    constexpr int XB = Pol::template x_bytes<B>();
+    constexpr uint32_t TX = Pol::template tx_bytes<B>();
+    const uint32_t n = (uint32_t)(cr.ce - cr.cs);
+    int pending = npre; // units requested and not yet consumed
+    for (uint32_t j = 0; pending > 0; ++j) {
+        const int s = (int)(j % NBUF);
+        const uint32_t st = stage0 + s * SB, bar = bar0 + 8 * s;
+        mbar_wait_bounded(bar, (j / NBUF) & 1u, p.scratch.status, dead);
+        const uint32_t u = qv.stage_unit[warp * NBUF + s];
+        typename Pol::template Regs<B> r;
+        Pol::template load<B>(stage0p + s * SB, lane, r);
+        __syncwarp(); // every lane's reads of the stage (and of its unit number) are done
+        uint32_t un = 0xFFFFFFFFu;
+        if (lane == 0 && !dead) {
+            un = atomicAdd(qv.claim, 1u);
+            if (un < n) {
+                int32_t rb, kc;
+                queue_unit_coords(p, cr.cs, un, rb, kc);
+                qv.stage_unit[warp * NBUF + s] = un;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, TX);
+                Pol::issue_weights(st, bar, kc, rb * kUnitRows, pol, *maps);
+                tma_load_2d(xr0 + ((j + NBUF) % (NBUF + 1)) * XB, &maps->x, kc * Pol::kCols, 0, bar);
+            } else {
+                un = 0xFFFFFFFFu;
+            }
+        }
+        un = __shfl_sync(0xFFFFFFFFu, un, 0);
+        if (un == 0xFFFFFFFFu)
+            --pending;
+        float acc[4][B];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                acc[q][b] = 0.f;
+        Pol::template compute<B>(r, xringp + (j % (NBUF + 1)) * XB, xfp, pol_smem, pst, lane, acc);
+        if (u < n)
+            qv.upart[u * 32 + lane] = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+    }
+}
+
+// After the CTA barrier: warp w adds the unit sums of the CTA's row blocks
+// w, w+W, ... in unit order (four interleaved partial sums, combined in a
+// fixed order) and finishes them.
+template <int B, int W, bool F32OUT>
+__device__ __forceinline__ void queue_finish(const StreamKParams &p, const CtaRange &cr, QueueView qv, int warp,
+                                             int lane)
+{
+    if (cr.ce <= cr.cs)
+        return;
+    const int64_t KC = p.KC;
+    const int64_t rbf = div64(cr.cs, KC), rbl = div64(cr.ce - 1, KC);
+    for (int64_t rb = rbf + warp; rb <= rbl; rb += W) {
+        const int64_t lo = (rb * KC > cr.cs ? rb * KC : cr.cs) - cr.cs;
+        const int64_t hi = ((rb + 1) * KC < cr.ce ? (rb + 1) * KC : cr.ce) - cr.cs;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        int64_t u = lo;
+        for (; u + 4 <= hi; u += 4) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                s4[t] += qv.upart[(u + t) * 32 + lane];
+        }
+        if (u < hi)
+            s4[0] += qv.upart[u * 32 + lane];
+        if (u + 1 < hi)
+            s4[1] += qv.upart[(u + 1) * 32 + lane];
+        if (u + 2 < hi)
+            s4[2] += qv.upart[(u + 2) * 32 + lane];
+        float tot[B];
+        tot[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        finish_across_ctas<B, F32OUT>(p, cr, rb, tot, lane);
+    }
+}
+
 template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
 __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_constant__ TensorMaps maps,
                                                                 const StreamKParams p)
@@ -443,11 +611,40 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
     const uint32_t bar0 = smem_addr(&full_bar[warp * NBUF]);
     const CtaRange cr = cta_range(p, W, blockIdx.x);
     const WarpWork w = warp_work(cr, p.KC, warp);
+    const uint64_t pol = l2_policy_evict_first();
+    bool dead = false;
+    typename Pol::State pst = Pol::initial_state();
+
+    if constexpr (B == 1) {
+        if (p.shared_queue) {
+            const QueueView qv = queue_view<Pol, B, W, NBUF>(sm.queue);
+            int npre = 0;
+            if (lane == 0) {
+                for (int i = 0; i < NBUF; ++i)
+                    mbar_init(bar0 + 8 * i, 1);
+                fence_mbar_init();
+                npre = queue_prologue<Pol, B, NBUF>(&maps, p, cr, qv, warp, stage0, bar0, pol);
+            }
+            if (threadIdx.x == 0)
+                *qv.claim = (uint32_t)(W * NBUF);
+            Pol::init_shared(sm.pol, threadIdx.x, W * 32); // overlaps the first weight copies
+            __syncthreads();
+            pdl_wait_upstream(); // x may be the previous kernel's output
+            if (lane == 0)
+                queue_prologue_x<Pol, B, NBUF>(&maps, p, cr, qv, warp, npre, xr0, bar0);
+            pdl_launch_dependents();
+            npre = __shfl_sync(0xFFFFFFFFu, npre, 0);
+            consume_queue<Pol, B, W, NBUF>(&maps, p, cr, qv, npre, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp,
+                                           sm.pol, warp, lane, pol, pst, dead);
+            __syncthreads(); // every unit sum of this CTA is in shared memory
+            queue_finish<B, W, F32OUT>(p, cr, qv, warp, lane);
+            return;
+        }
+    }
 
     // Each warp's barriers are its own (initialised, armed and waited on by
     // the warp): the weights of its first stages, which do not depend on the
     // previous kernel, are requested before anything else.
-    const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
         for (int i = 0; i < NBUF; ++i)
             mbar_init(bar0 + 8 * i, 1);
@@ -462,8 +659,6 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
         issue_prologue_x<Pol, B, NBUF>(&maps, w, p.KC, 0, xr0, bar0);
     pdl_launch_dependents();
 
-    bool dead = false;
-    typename Pol::State pst = Pol::initial_state();
     consume_range<Pol, B, W, NBUF, F32OUT>(&maps, p, w, 0, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp, sm.pol,
                                            sm.part, warp,
                                            lane, pol, pst, dead);
@@ -496,6 +691,8 @@ __device__ __forceinline__ StreamKParams op_params(const StackOp *op, const Scra
     p.KC = op->KC;
     p.whole = op->whole;
     p.P = op->P;
+    p.shared_queue = 0; // the persistent kernel splits each op statically
+    p.kc_inv = 0;
     p.scratch = scratch;
     return p;
 }
@@ -685,6 +882,10 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     p.whole = sp.whole ? 1 : 0;
     p.P = (int32_t)sp.ctas;
     const int64_t ctas = sp.ctas;
+    // the shared queue when every CTA's range fits it (and unit numbers stay small)
+    const int64_t most = sp.whole ? ((nrb + ctas - 1) / ctas) * KC : (p.U + ctas - 1) / ctas;
+    p.shared_queue = (B == 1 && most <= queue_cap<W>() && KC >= 2 && KC < 32768) ? 1 : 0;
+    p.kc_inv = (uint32_t)((((uint64_t)1 << 32) + KC - 1) / KC);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
