@@ -466,14 +466,27 @@ __device__ __forceinline__ QueueView queue_view(uint8_t *q)
     return v;
 }
 
-// Row block and position of unit u of the CTA range starting at unit cs.
-__device__ __forceinline__ void queue_unit_coords(const StreamKParams &p, int64_t cs, uint32_t u, int32_t &rb,
+// Where the CTA range starts: row block rb_cs, position kc_cs in it.
+struct QueueBase {
+    int32_t rb_cs;
+    uint32_t kc_cs;
+};
+
+__device__ __forceinline__ QueueBase queue_base(const StreamKParams &p, int64_t cs)
+{
+    QueueBase qb;
+    qb.rb_cs = (int32_t)div64(cs, p.KC);
+    qb.kc_cs = (uint32_t)(cs - (int64_t)qb.rb_cs * p.KC);
+    return qb;
+}
+
+// Row block and position of unit u of the CTA range.
+__device__ __forceinline__ void queue_unit_coords(const StreamKParams &p, QueueBase qb, uint32_t u, int32_t &rb,
                                                   int32_t &kc)
 {
-    const int32_t rb_cs = (int32_t)div64(cs, p.KC);
-    const uint32_t k = (uint32_t)(cs - (int64_t)rb_cs * p.KC) + u; // < KC + cap
+    const uint32_t k = qb.kc_cs + u; // < KC + cap
     const uint32_t q = __umulhi(k, p.kc_inv);
-    rb = rb_cs + (int32_t)q;
+    rb = qb.rb_cs + (int32_t)q;
     kc = (int32_t)(k - q * (uint32_t)p.KC);
 }
 
@@ -485,13 +498,14 @@ __device__ __forceinline__ int queue_prologue(const TensorMaps *maps, const Stre
     constexpr int SB = Pol::template stage_bytes<B>();
     constexpr uint32_t TX = Pol::template tx_bytes<B>();
     const uint32_t n = (uint32_t)(cr.ce - cr.cs);
+    const QueueBase qb = queue_base(p, cr.cs);
     int npre = 0;
     for (int i = 0; i < NBUF; ++i) {
         const uint32_t u = (uint32_t)(warp * NBUF + i);
         if (u >= n)
             break;
         int32_t rb, kc;
-        queue_unit_coords(p, cr.cs, u, rb, kc);
+        queue_unit_coords(p, qb, u, rb, kc);
         qv.stage_unit[warp * NBUF + i] = u;
         mbar_arrive_expect_tx(bar0 + 8 * i, TX);
         Pol::issue_weights(stage0 + i * SB, bar0 + 8 * i, kc, rb * kUnitRows, pol, *maps);
@@ -506,9 +520,10 @@ __device__ __forceinline__ void queue_prologue_x(const TensorMaps *maps, const S
                                                  QueueView qv, int warp, int npre, uint32_t xr0, uint32_t bar0)
 {
     constexpr int XB = Pol::template x_bytes<B>();
+    const QueueBase qb = queue_base(p, cr.cs);
     for (int i = 0; i < npre; ++i) {
         int32_t rb, kc;
-        queue_unit_coords(p, cr.cs, qv.stage_unit[warp * NBUF + i], rb, kc);
+        queue_unit_coords(p, qb, qv.stage_unit[warp * NBUF + i], rb, kc);
         tma_load_2d(xr0 + i * XB, &maps->x, kc * Pol::kCols, 0, bar0 + 8 * i);
     }
 }
@@ -524,8 +539,11 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
     constexpr int XB = Pol::template x_bytes<B>();
     constexpr uint32_t TX = Pol::template tx_bytes<B>();
     const uint32_t n = (uint32_t)(cr.ce - cr.cs);
+    const QueueBase qb = queue_base(p, cr.cs);
     int pending = npre; // units requested and not yet consumed
+    uint32_t xs = 0;    // x slot of unit j: j % (NBUF + 1)
     for (uint32_t j = 0; pending > 0; ++j) {
+        const uint32_t xn = xs == 0 ? NBUF : xs - 1; // x slot of unit j + NBUF
         const int s = (int)(j % NBUF);
         const uint32_t st = stage0 + s * SB, bar = bar0 + 8 * s;
         mbar_wait_bounded(bar, (j / NBUF) & 1u, p.scratch.status, dead);
@@ -538,12 +556,12 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
             un = atomicAdd(qv.claim, 1u);
             if (un < n) {
                 int32_t rb, kc;
-                queue_unit_coords(p, cr.cs, un, rb, kc);
+                queue_unit_coords(p, qb, un, rb, kc);
                 qv.stage_unit[warp * NBUF + s] = un;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, TX);
                 Pol::issue_weights(st, bar, kc, rb * kUnitRows, pol, *maps);
-                tma_load_2d(xr0 + ((j + NBUF) % (NBUF + 1)) * XB, &maps->x, kc * Pol::kCols, 0, bar);
+                tma_load_2d(xr0 + xn * XB, &maps->x, kc * Pol::kCols, 0, bar);
             } else {
                 un = 0xFFFFFFFFu;
             }
@@ -557,9 +575,10 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
 #pragma unroll
             for (int b = 0; b < B; ++b)
                 acc[q][b] = 0.f;
-        Pol::template compute<B>(r, xringp + (j % (NBUF + 1)) * XB, xfp, pol_smem, pst, lane, acc);
+        Pol::template compute<B>(r, xringp + xs * XB, xfp, pol_smem, pst, lane, acc);
         if (u < n)
             qv.upart[u * 32 + lane] = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+        xs = xs == NBUF ? 0 : xs + 1;
     }
 }
 
