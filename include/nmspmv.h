@@ -152,16 +152,22 @@ typedef struct nm_linear {
     const void *values; /* bf16 [rows][K/2] */
     const void *W;      /* bf16 [rows][K] */
     const void *x;      /* bf16 [batch][K] */
-    void *y;            /* bf16 [batch][rows] */
+    void *y;            /* bf16 [batch][rows] ([batch][rows/2] with NM_LINEAR_SWIGLU) */
     int64_t rows;
     int64_t K;
+    uint32_t flags;     /* 0, or NM_LINEAR_SWIGLU (sparse ops only) */
 } nm_linear;
+
+/* The op is a gate/up pair matrix in the pair layout of nm_pack_swiglu
+ * (rows = 2 * rows_h, a multiple of 32) and stores h as nm_spmv_swiglu does. */
+#define NM_LINEAR_SWIGLU 1u
 
 /*
  * nm_spmv_stack / dense_gemv_stack -- the linear stack of one decode token
  * (every pruned linear of every layer; only linear layers are sparse, per the
  * ai.info summary, "Methodology" step 4 and paper.rainbus.top "局限与改进").
- * Runs ops[0..n_ops) in order on `stream`, each as nm_spmv / dense_gemv.
+ * Runs ops[0..n_ops) in order on `stream`, each as nm_spmv / dense_gemv (an op
+ * with NM_LINEAR_SWIGLU as nm_spmv_swiglu; dense ops take flags 0).
  * Consecutive launches are chained with programmatic dependent launch: a
  * kernel may start streaming its own weights before the previous one ends,
  * but reads its x only after the previous kernel has completed, exactly as if
@@ -170,6 +176,32 @@ typedef struct nm_linear {
  */
 nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
 nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream);
+
+/*
+ * nm_pack_swiglu / nm_spmv_swiglu -- an MLP's gate and up projections as one
+ * SpMV whose epilogue applies the SwiGLU activation, so that its output h is
+ * directly the x of the down projection. Not described on the pages, whose
+ * kernel is the plain SpMV; this is the step after it in a decode layer (only
+ * the linear layers are pruned: ai.info summary, "Methodology in Plain
+ * English" step 4).
+ *
+ * Pair layout: the packed matrix has 2 * rows_h rows; row block t (rows 32t ..
+ * 32t+31) holds gate rows 16t .. 16t+15 followed by up rows 16t .. 16t+15, so
+ * that each gate row and its up row meet in one row block.
+ *   nm_pack_swiglu: W_gate, W_up: device bf16 [rows_h][K], pruned (read);
+ *     masks: uint32 [2*rows_h][K/32], values: bf16 [2*rows_h][K/2] (written)
+ *     in the pair layout. rows_h % 16 == 0 (NM_ERR_SHAPE). Otherwise as
+ *     nm_pack (synchronous; NM_ERR_NOT_NM as there).
+ *   nm_spmv_swiglu: masks, values in the pair layout; x: bf16 [batch][K];
+ *     h: bf16 [batch][rows_h] (written) with
+ *       g = sum_j W_gate[r][j] x[b][j],  u = sum_j W_up[r][j] x[b][j]  (fp32),
+ *       h[b][r] = bf16_rn(g / (1 + exp(-g)) * u)                       (fp32).
+ *     rows_h % 16 == 0 (NM_ERR_SHAPE). Otherwise as nm_spmv (asynchronous).
+ */
+nm_status nm_pack_swiglu(const void *W_gate_bf16, const void *W_up_bf16, int64_t rows_h, int64_t K, int N, int M,
+                         uint32_t *masks, void *values_bf16, void *stream);
+nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *h_bf16,
+                         int64_t rows_h, int64_t K, int batch, void *stream);
 
 /*
  * nm_stack_plan -- a decode-token stack prepared once, run many times.

@@ -57,7 +57,10 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_pack.argtypes = [p, i64, i64, i32, i32, p, p]
         _lib.oracle_unpack.argtypes = [p, p, i64, i64, p]
         _lib.oracle_spmv_f64.argtypes = [p, p, i64, i64, i32, p, p]
-        for f in (_lib.oracle_select, _lib.oracle_pack, _lib.oracle_unpack, _lib.oracle_spmv_f64):
+        _lib.oracle_swiglu_f64.argtypes = [p, p, i64, p]
+        _lib.oracle_pair_rows.argtypes = [p, p, i64, i64, p]
+        for f in (_lib.oracle_select, _lib.oracle_pack, _lib.oracle_unpack, _lib.oracle_spmv_f64,
+                  _lib.oracle_swiglu_f64, _lib.oracle_pair_rows):
             f.restype = ctypes.c_int
     return _lib
 
@@ -132,3 +135,31 @@ def spmv_f64(W_bits, x_bits):
 def spmv_packed_f64(masks, values, x_bits, K: int):
     """The oracle's product from the packed format: decode, then the dense fp64 product."""
     return spmv_f64(unpack(masks, values, K), x_bits)
+
+
+def swiglu_f64(g, u) -> np.ndarray:
+    """h = silu(g) * u elementwise in fp64, silu(g) = g / (1 + exp(-g))."""
+    g = np.ascontiguousarray(np.asarray(g, dtype=np.float64))
+    u = np.ascontiguousarray(np.asarray(u, dtype=np.float64))
+    assert g.shape == u.shape
+    h = np.empty_like(g)
+    _check(lib().oracle_swiglu_f64(_ptr(g), _ptr(u), g.size, _ptr(h)), "oracle_swiglu_f64")
+    return h
+
+
+def pair_rows(Wg_bits, Wu_bits) -> np.ndarray:
+    """The pair layout: row block t holds gate rows 16t..16t+15, then up rows 16t..16t+15."""
+    Wg_bits = _u16(Wg_bits)
+    Wu_bits = _u16(Wu_bits)
+    assert Wg_bits.shape == Wu_bits.shape
+    rows_h, K = Wg_bits.shape
+    out = np.empty((2 * rows_h, K), dtype=np.uint16)
+    _check(lib().oracle_pair_rows(_ptr(Wg_bits), _ptr(Wu_bits), rows_h, K, _ptr(out)), "oracle_pair_rows")
+    return out
+
+
+def spmv_swiglu_f64(Wg_bits, Wu_bits, x_bits):
+    """The fused gate/up SpMV with SwiGLU: (h, g, u, Sg, Su), each [batch][rows_h] float64."""
+    g, Sg = spmv_f64(Wg_bits, x_bits)
+    u, Su = spmv_f64(Wu_bits, x_bits)
+    return swiglu_f64(g, u), g, u, Sg, Su

@@ -230,3 +230,39 @@ int oracle_spmv_f64(const uint16_t *W, const uint16_t *x, int64_t rows, int64_t 
     }
     return OR_OK;
 }
+
+/*
+ * SwiGLU of an MLP's gate and up products (the step after the SpMV in a
+ * decode layer; the pages prune only the linear layers): h = silu(g) * u with
+ * silu(g) = g / (1 + e^-g), all in fp64, elementwise over n values.
+ */
+int oracle_swiglu_f64(const double *g, const double *u, int64_t n, double *h)
+{
+    if (n < 0)
+        return OR_BAD_SHAPE;
+    if (n > 0 && (!g || !u || !h))
+        return OR_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+    return OR_OK;
+}
+
+/*
+ * The pair layout of a gate/up matrix: row block t (rows 32t .. 32t+31) holds
+ * gate rows 16t .. 16t+15, then up rows 16t .. 16t+15. Copies bf16 bits.
+ */
+int oracle_pair_rows(const uint16_t *Wg, const uint16_t *Wu, int64_t rows_h, int64_t K, uint16_t *out)
+{
+    if (rows_h < 0 || K < 0 || rows_h % 16 != 0)
+        return OR_BAD_SHAPE;
+    if (rows_h > 0 && K > 0 && (!Wg || !Wu || !out))
+        return OR_BAD_ARG;
+    for (int64_t r = 0; r < rows_h; ++r) {
+        const int64_t og = (r / 16) * 32 + r % 16, ou = og + 16;
+        for (int64_t j = 0; j < K; ++j) {
+            out[og * K + j] = Wg[r * K + j];
+            out[ou * K + j] = Wu[r * K + j];
+        }
+    }
+    return OR_OK;
+}

@@ -31,12 +31,13 @@ PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 
 NM_STACK_DENSE = 1
 NM_STACK_PERSISTENT = 2
+NM_LINEAR_SWIGLU = 1
 
 # Every symbol the header declares (the CPU test checks they are exported).
 EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
            "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
-           "nm_stack_plan_destroy")
+           "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu")
 
 
 class NmError(RuntimeError):
@@ -49,7 +50,7 @@ class NmLinear(ctypes.Structure):
     """Mirror of ``nm_linear`` in include/nmspmv.h."""
     _fields_ = [("masks", ctypes.c_void_p), ("values", ctypes.c_void_p), ("W", ctypes.c_void_p),
                 ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("K", ctypes.c_int64)]
+                ("K", ctypes.c_int64), ("flags", ctypes.c_uint32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
         "nm_stack_plan_create": ([ctypes.POINTER(NmLinear), i32, i32, ctypes.c_uint, ctypes.POINTER(p)], i32),
         "nm_stack_plan_run": ([p, p], i32),
         "nm_stack_plan_destroy": ([p], i32),
+        "nm_pack_swiglu": ([p, p, i64, i64, i32, i32, p, p, p], i32),
+        "nm_spmv_swiglu": ([p, p, p, p, i64, i64, i32, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -184,6 +187,39 @@ def spmv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, out: Option
     return out
 
 
+def pack_swiglu(W_gate: torch.Tensor, W_up: torch.Tensor, N: int, M: int):
+    """Pruned gate and up matrices (bf16, CUDA, [rows_h][K]) -> (masks, values) in the pair
+    layout of nm_pack_swiglu: [2*rows_h][K/32] and [2*rows_h][K/2]."""
+    _cuda(W_gate, torch.bfloat16, "W_gate")
+    _cuda(W_up, torch.bfloat16, "W_up")
+    if W_gate.shape != W_up.shape:
+        raise ValueError("W_gate and W_up must have the same shape")
+    rows_h, K = W_gate.shape
+    masks = torch.empty(2 * rows_h, K // 32, dtype=torch.int32, device=W_gate.device)
+    values = torch.empty(2 * rows_h, K // 2, dtype=torch.bfloat16, device=W_gate.device)
+    _check(lib().nm_pack_swiglu(W_gate.data_ptr(), W_up.data_ptr(), rows_h, K, N, M, masks.data_ptr(),
+                                values.data_ptr(), ctypes.c_void_p(_stream(W_gate))), "nm_pack_swiglu")
+    return masks, values
+
+
+def spmv_swiglu(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """h[b][r] = bf16(silu(g) * u), g and u the gate and up rows of a pair-layout matrix times x."""
+    _cuda(masks, torch.int32, "masks")
+    _cuda(values, torch.bfloat16, "values")
+    x = _cuda(_x2d(x), torch.bfloat16, "x")
+    rows = masks.shape[0]
+    K = masks.shape[1] * 32
+    batch = x.shape[0]
+    if values.shape != (rows, K // 2) or x.shape[1] != K or rows % 32 != 0:
+        raise ValueError("shape mismatch between masks, values and x (rows must be a multiple of 32)")
+    out = torch.empty(batch, rows // 2, dtype=torch.bfloat16, device=x.device) if out is None else \
+        _cuda(out, torch.bfloat16, "out")
+    _check(lib().nm_spmv_swiglu(masks.data_ptr(), values.data_ptr(), x.data_ptr(), out.data_ptr(), rows // 2, K,
+                                batch, ctypes.c_void_p(_stream(x))), "nm_spmv_swiglu")
+    return out
+
+
 def dense_gemv(W: torch.Tensor, x: torch.Tensor, out: Optional[torch.Tensor] = None,
                f32: bool = False) -> torch.Tensor:
     """Dense bf16 reference: y[b][r] = sum_j W[r][j] x[b][j]."""
@@ -210,6 +246,7 @@ def _linear_array(ops: Sequence[dict]) -> ctypes.Array:
             setattr(t, f, v.data_ptr() if v is not None else None)
         t.rows = int(op["rows"])
         t.K = int(op["K"])
+        t.flags = int(op.get("flags", 0))
     return arr
 
 

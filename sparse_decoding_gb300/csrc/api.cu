@@ -98,26 +98,80 @@ static nm_status check_gemv_args(const void *W, const void *x, const void *y, in
     return NM_OK;
 }
 
+// One op of a stack: the checks of its call, and its flags.
+static nm_status check_stack_op(const nm_linear &o, bool dense, int batch)
+{
+    if (o.flags & ~(uint32_t)NM_LINEAR_SWIGLU)
+        return NM_ERR_INVALID_ARG;
+    if (dense) {
+        if (o.flags)
+            return NM_ERR_INVALID_ARG;
+        return check_gemv_args(o.W, o.x, o.y, o.rows, o.K, batch);
+    }
+    if ((o.flags & NM_LINEAR_SWIGLU) && o.rows % 32 != 0)
+        return NM_ERR_SHAPE;
+    return check_spmv_args(o.masks, o.values, o.x, o.y, o.rows, o.K, batch);
+}
+
 static nm_status zero_output(void *y, int64_t rows, int batch, size_t elt, cudaStream_t stream)
 {
     return cudaMemsetAsync(y, 0, (size_t)rows * batch * elt, stream) == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
-static nm_status spmv_impl(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,
-                           int64_t rows, int64_t K, int batch, cudaStream_t stream, bool pdl)
+// out: kOutBf16, kOutF32, or kOutSwiglu (rows = gate/up pair rows, y = h [batch][rows / 2]).
+static nm_status spmv_impl(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
+                           int64_t K, int batch, cudaStream_t stream, bool pdl)
 {
     nm_status s = check_spmv_args(masks, values, x, y, rows, K, batch);
     if (s != NM_OK || rows == 0)
         return s;
+    if (out == kOutSwiglu && rows % 32 != 0)
+        return NM_ERR_SHAPE;
     if (K == 0)
-        return zero_output(y, rows, batch, f32out ? 4 : 2, stream);
+        return out == kOutSwiglu ? zero_output(y, rows / 2, batch, 2, stream)
+                                 : zero_output(y, rows, batch, out == kOutF32 ? 4 : 2, stream);
     LaunchCtx ctx;
     if ((s = device_ctx(stream, pdl, &ctx)) != NM_OK)
         return s;
-    s = launch_spmv(masks, values, x, y, f32out, rows, K, batch, ctx);
+    s = launch_spmv(masks, values, x, y, out, rows, K, batch, ctx);
     if (s == NM_OK && cudaGetLastError() != cudaSuccess)
         s = NM_ERR_CUDA;
     return s;
+}
+
+// Pack Wa (Wb == NULL), or the gate/up pair Wa, Wb (rows rows each) into the pair layout.
+static nm_status pack_impl(const void *Wa, const void *Wb, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
+                           void *values_bf16, void *stream)
+{
+    if (!pattern_ok(N, M))
+        return NM_ERR_UNSUPPORTED;
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (rows == 0 || K == 0)
+        return NM_OK;
+    if (!Wa || !masks || !values_bf16)
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(Wa) || (Wb && !aligned16(Wb)) || !aligned16(masks) || !aligned16(values_bf16))
+        return NM_ERR_ALIGN;
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    // One pack at a time per process: the error flag lives in the shared scratch.
+    static std::mutex pack_mu;
+    std::lock_guard<std::mutex> lock(pack_mu);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ctx.scratch.status + 1, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    if ((s = launch_pack(Wa, rows, K, N, M, masks, values_bf16, ctx, Wb ? 0 : -1)) != NM_OK)
+        return s;
+    if (Wb && (s = launch_pack(Wb, rows, K, N, M, masks, values_bf16, ctx, 16)) != NM_OK)
+        return s;
+    uint32_t bad = 0;
+    if (cudaMemcpyAsync(&bad, ctx.scratch.status + 1, sizeof bad, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    return bad ? NM_ERR_NOT_NM : NM_OK;
 }
 
 static nm_status gemv_impl(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K, int batch,
@@ -157,7 +211,7 @@ struct nm_stack_plan {
 
 extern "C" {
 
-int nm_abi_version(void) { return 1; }
+int nm_abi_version(void) { return 2; }
 
 const char *nm_status_str(int status)
 {
@@ -197,45 +251,38 @@ nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K,
 nm_status nm_pack(const void *W_bf16, int64_t rows, int64_t K, int N, int M, uint32_t *masks, void *values_bf16,
                   void *stream)
 {
-    if (!pattern_ok(N, M))
-        return NM_ERR_UNSUPPORTED;
-    if (rows < 0 || K < 0 || (K % 32) != 0)
+    return pack_impl(W_bf16, nullptr, rows, K, N, M, masks, values_bf16, stream);
+}
+
+nm_status nm_pack_swiglu(const void *W_gate_bf16, const void *W_up_bf16, int64_t rows_h, int64_t K, int N, int M,
+                         uint32_t *masks, void *values_bf16, void *stream)
+{
+    if (rows_h % 16 != 0)
         return NM_ERR_SHAPE;
-    if (rows == 0 || K == 0)
-        return NM_OK;
-    if (!W_bf16 || !masks || !values_bf16)
+    if (rows_h > 0 && K > 0 && !W_up_bf16)
         return NM_ERR_INVALID_ARG;
-    if (!aligned16(W_bf16) || !aligned16(masks) || !aligned16(values_bf16))
-        return NM_ERR_ALIGN;
-    LaunchCtx ctx;
-    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
-    if (s != NM_OK)
-        return s;
-    // One pack at a time per process: the error flag lives in the shared scratch.
-    static std::mutex pack_mu;
-    std::lock_guard<std::mutex> lock(pack_mu);
-    cudaStream_t st = (cudaStream_t)stream;
-    if (cudaMemsetAsync(ctx.scratch.status + 1, 0, sizeof(uint32_t), st) != cudaSuccess)
-        return NM_ERR_CUDA;
-    if ((s = launch_pack(W_bf16, rows, K, N, M, masks, values_bf16, ctx)) != NM_OK)
-        return s;
-    uint32_t bad = 0;
-    if (cudaMemcpyAsync(&bad, ctx.scratch.status + 1, sizeof bad, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return NM_ERR_CUDA;
-    return bad ? NM_ERR_NOT_NM : NM_OK;
+    return pack_impl(W_gate_bf16, W_up_bf16, rows_h, K, N, M, masks, values_bf16, stream);
+}
+
+nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *h_bf16,
+                         int64_t rows_h, int64_t K, int batch, void *stream)
+{
+    if (rows_h < 0 || rows_h % 16 != 0)
+        return NM_ERR_SHAPE;
+    return spmv_impl(masks, values_bf16, x_bf16, h_bf16, kOutSwiglu, 2 * rows_h, K, batch, (cudaStream_t)stream,
+                     false);
 }
 
 nm_status nm_spmv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *y_bf16, int64_t rows,
                   int64_t K, int batch, void *stream)
 {
-    return spmv_impl(masks, values_bf16, x_bf16, y_bf16, false, rows, K, batch, (cudaStream_t)stream, false);
+    return spmv_impl(masks, values_bf16, x_bf16, y_bf16, kOutBf16, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
                          int64_t rows, int64_t K, int batch, void *stream)
 {
-    return spmv_impl(masks, values_bf16, x_bf16, y_f32, true, rows, K, batch, (cudaStream_t)stream, false);
+    return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status dense_gemv(const void *W_bf16, const void *x_bf16, void *y_bf16, int64_t rows, int64_t K, int batch,
@@ -255,12 +302,13 @@ nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream
     if (n_ops < 0 || (n_ops > 0 && !ops))
         return NM_ERR_INVALID_ARG;
     for (int i = 0; i < n_ops; ++i) {
-        nm_status s = check_spmv_args(ops[i].masks, ops[i].values, ops[i].x, ops[i].y, ops[i].rows, ops[i].K, batch);
+        nm_status s = check_stack_op(ops[i], false, batch);
         if (s != NM_OK)
             return s;
     }
     for (int i = 0; i < n_ops; ++i) {
-        nm_status s = spmv_impl(ops[i].masks, ops[i].values, ops[i].x, ops[i].y, false, ops[i].rows, ops[i].K, batch,
+        nm_status s = spmv_impl(ops[i].masks, ops[i].values, ops[i].x, ops[i].y,
+                                (ops[i].flags & NM_LINEAR_SWIGLU) ? kOutSwiglu : kOutBf16, ops[i].rows, ops[i].K, batch,
                                 (cudaStream_t)stream, true);
         if (s != NM_OK)
             return s;
@@ -273,7 +321,7 @@ nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *str
     if (n_ops < 0 || (n_ops > 0 && !ops))
         return NM_ERR_INVALID_ARG;
     for (int i = 0; i < n_ops; ++i) {
-        nm_status s = check_gemv_args(ops[i].W, ops[i].x, ops[i].y, ops[i].rows, ops[i].K, batch);
+        nm_status s = check_stack_op(ops[i], true, batch);
         if (s != NM_OK)
             return s;
     }
@@ -294,11 +342,12 @@ nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsig
     bool fits = n_ops > 0 && (flags & NM_STACK_PERSISTENT);
     for (int i = 0; i < n_ops; ++i) {
         const nm_linear &o = ops[i];
-        nm_status s = dense ? check_gemv_args(o.W, o.x, o.y, o.rows, o.K, batch)
-                            : check_spmv_args(o.masks, o.values, o.x, o.y, o.rows, o.K, batch);
+        nm_status s = check_stack_op(o, dense, batch);
         if (s != NM_OK)
             return s;
-        fits = fits && (dense ? gemv_tma_ok(o.rows, o.K) : (o.rows > 0 && o.K > 0 && spmv_path(o.rows, o.K) == kSpmvTma));
+        // the persistent kernel stores plain bf16 y only
+        fits = fits && o.flags == 0 &&
+               (dense ? gemv_tma_ok(o.rows, o.K) : (o.rows > 0 && o.K > 0 && spmv_path(o.rows, o.K) == kSpmvTma));
     }
     if (n_ops == 0 && (batch < 1 || batch > 8))
         return NM_ERR_UNSUPPORTED;

@@ -20,7 +20,7 @@ namespace nm {
 constexpr int kGemvWarps = 16;
 constexpr int kGemvUnroll = 8;
 
-template <int B, bool F32OUT>
+template <int B, int OUT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_kernel(const uint16_t *__restrict__ W, const uint16_t *__restrict__ x, void *y, int64_t rows,
                 int64_t K)
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
         if (lane == 0) {
 #pragma unroll
             for (int b = 0; b < B; ++b) {
-                if (F32OUT)
+                if (OUT)
                     ((float *)y)[(int64_t)b * rows + row] = acc[b];
                 else
                     ((uint16_t *)y)[(int64_t)b * rows + row] = f32_to_bf16_rn(acc[b]);
@@ -184,7 +184,7 @@ static nm_status encode_dense_maps(const void *W, const void *x, int64_t rows, i
                      kDnCols, B, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int B, bool F32OUT>
+template <int B, int OUT>
 static nm_status launch_gemv_tma(const void *W, const void *x, void *y, int64_t rows, int64_t K,
                                  const LaunchCtx &ctx)
 {
@@ -195,13 +195,13 @@ static nm_status launch_gemv_tma(const void *W, const void *x, void *y, int64_t 
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kDnCols;
     if constexpr (B <= 2) {
         if (nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
-            return launch_streamk<DenseUnit, B, 16, 2, 1, F32OUT>(maps, y, rows, KC, ctx);
+            return launch_streamk<DenseUnit, B, 16, 2, 1, OUT>(maps, y, rows, KC, ctx);
     }
-    return launch_streamk<DenseUnit, B, DenseCfg<B>::W, DenseCfg<B>::NBUF, DenseCfg<B>::MINB, F32OUT>(
+    return launch_streamk<DenseUnit, B, DenseCfg<B>::W, DenseCfg<B>::NBUF, DenseCfg<B>::MINB, OUT>(
         maps, y, rows, KC, ctx);
 }
 
-template <int B, bool F32OUT>
+template <int B, int OUT>
 static nm_status launch_gemv_b(const void *W, const void *x, void *y, int64_t rows, int64_t K,
                                const LaunchCtx &ctx)
 {
@@ -217,20 +217,20 @@ static nm_status launch_gemv_b(const void *W, const void *x, void *y, int64_t ro
     attr[0].val.programmaticStreamSerializationAllowed = ctx.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_kernel<B, F32OUT>, (const uint16_t *)W, (const uint16_t *)x, y, rows, K) !=
+    if (cudaLaunchKernelEx(&cfg, gemv_kernel<B, OUT>, (const uint16_t *)W, (const uint16_t *)x, y, rows, K) !=
         cudaSuccess)
         return NM_ERR_CUDA;
     return NM_OK;
 }
 
-template <bool F32OUT>
+template <int OUT>
 static nm_status gemv_dispatch(const void *W, const void *x, void *y, int64_t rows, int64_t K, int batch,
                                const LaunchCtx &ctx)
 {
     const bool tma = K % kDnCols == 0 && rows <= 0x7FFFFFFF && K <= 0x7FFFFFFF;
 #define NM_CASE(BB)                                                                                         \
     case BB:                                                                                                \
-        return tma ? launch_gemv_tma<BB, F32OUT>(W, x, y, rows, K, ctx) : launch_gemv_b<BB, F32OUT>(W, x, y, rows, K, ctx);
+        return tma ? launch_gemv_tma<BB, OUT>(W, x, y, rows, K, ctx) : launch_gemv_b<BB, OUT>(W, x, y, rows, K, ctx);
     switch (batch) {
         NM_CASE(1)
         NM_CASE(2)
@@ -285,8 +285,8 @@ nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t 
 nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K, int batch,
                       const LaunchCtx &ctx)
 {
-    return f32out ? gemv_dispatch<true>(W, x, y, rows, K, batch, ctx)
-                  : gemv_dispatch<false>(W, x, y, rows, K, batch, ctx);
+    return f32out ? gemv_dispatch<kOutF32>(W, x, y, rows, K, batch, ctx)
+                  : gemv_dispatch<kOutBf16>(W, x, y, rows, K, batch, ctx);
 }
 
 } // namespace nm

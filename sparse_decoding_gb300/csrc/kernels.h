@@ -24,14 +24,20 @@ SpmvPath spmv_path(int64_t rows, int64_t K);
 // Largest grid (CTAs) the SpMV launches on a device with `num_sms` SMs.
 int spmv_max_ctas(int num_sms);
 
-nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,
-                      int64_t rows, int64_t K, int batch, const LaunchCtx &ctx);
+// What the SpMV stores: y in bf16, y in fp32, or (gate/up row pairs, see
+// nm_spmv_swiglu) h = silu(gate) * up in bf16.
+enum OutMode { kOutBf16 = 0, kOutF32 = 1, kOutSwiglu = 2 };
+
+nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
+                      int64_t K, int batch, const LaunchCtx &ctx);
 nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_t rows, int64_t K,
                       int batch, const LaunchCtx &ctx);
 nm_status launch_select(const void *W, const float *a, int64_t rows, int64_t K, int N, int M,
                         void *out, const LaunchCtx &ctx);
+// pair_off < 0: row r of W is row r of the output; 0 / 16: row r goes to
+// (r / 16) * 32 + r % 16 + pair_off (the gate / up half of the pair layout).
 nm_status launch_pack(const void *W, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
-                      void *values, const LaunchCtx &ctx);
+                      void *values, const LaunchCtx &ctx, int pair_off = -1);
 
 // The persistent stack kernel: a whole decode-token stack in one launch
 // (spmv.cu for sparse linears, gemv.cu for dense ones). Only shapes on the

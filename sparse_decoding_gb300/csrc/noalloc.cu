@@ -94,7 +94,7 @@ extern "C" nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_b
     // The array keeps whatever the previous call left; the counters must start at zero.
     if (cudaMemsetAsync(ctx.scratch.counters, 0, sizeof(uint32_t) * kNoAllocMaxCtas, st) != cudaSuccess)
         return NM_ERR_CUDA;
-    s = launch_spmv(masks, values_bf16, x_bf16, y_bf16, false, rows, K, batch, ctx);
+    s = launch_spmv(masks, values_bf16, x_bf16, y_bf16, kOutBf16, rows, K, batch, ctx);
     if (s == NM_OK && cudaGetLastError() != cudaSuccess)
         s = NM_ERR_CUDA;
     return s;

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kPackThreads)
 template <int M>
 __global__ void __launch_bounds__(kPackThreads)
     pack_kernel(const uint16_t *__restrict__ W, int64_t rows, int64_t K, int N, uint32_t *masks, uint16_t *values,
-                uint32_t *bad)
+                uint32_t *bad, int pair_off)
 {
     __shared__ uint16_t col[32][kPackThreads]; // [column][thread]: private to each thread
     const int64_t words = K / 32;
@@ -145,10 +145,12 @@ __global__ void __launch_bounds__(kPackThreads)
         m &= m - 1;
         o[k >> 1] = (uint32_t)col[p0][threadIdx.x] | ((uint32_t)col[p1][threadIdx.x] << 16);
     }
-    uint4 *vp = (uint4 *)(values + row * (K / 2) + 16 * g);
+    // output row: the input row, or its slot in the gate/up pair layout
+    const int64_t orow = pair_off < 0 ? row : (row >> 4) * 32 + (row & 15) + pair_off;
+    uint4 *vp = (uint4 *)(values + orow * (K / 2) + 16 * g);
     vp[0] = make_uint4(o[0], o[1], o[2], o[3]);
     vp[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    masks[row * words + g] = mask;
+    masks[orow * words + g] = mask;
 }
 
 static int64_t grid_for(int64_t items)
@@ -179,7 +181,7 @@ nm_status launch_select(const void *W, const float *a, int64_t rows, int64_t K, 
 }
 
 nm_status launch_pack(const void *W, int64_t rows, int64_t K, int N, int M, uint32_t *masks, void *values,
-                      const LaunchCtx &ctx)
+                      const LaunchCtx &ctx, int pair_off)
 {
     const int64_t items = rows * (K / 32);
     if (items == 0)
@@ -192,10 +194,10 @@ nm_status launch_pack(const void *W, int64_t rows, int64_t K, int N, int M, uint
     uint16_t *v = (uint16_t *)values;
     uint32_t *bad = ctx.scratch.status + 1;
     switch (M) {
-    case 4: pack_kernel<4><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad); break;
-    case 8: pack_kernel<8><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad); break;
-    case 16: pack_kernel<16><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad); break;
-    case 32: pack_kernel<32><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad); break;
+    case 4: pack_kernel<4><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad, pair_off); break;
+    case 8: pack_kernel<8><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad, pair_off); break;
+    case 16: pack_kernel<16><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad, pair_off); break;
+    case 32: pack_kernel<32><<<gr, bl, 0, ctx.stream>>>(w, rows, K, N, masks, v, bad, pair_off); break;
     default: return NM_ERR_UNSUPPORTED;
     }
     return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;

@@ -298,7 +298,7 @@ template <int B> struct SparseCfg {
 // ---------------------------------------------------------------------------
 // Fallback: lane-per-row walk with plain global loads (any K % 32 == 0).
 // ---------------------------------------------------------------------------
-template <int B, bool F32OUT>
+template <int B, int OUT>
 __global__ void __launch_bounds__(256)
     spmv_simple_kernel(const uint32_t *__restrict__ masks, const uint16_t *__restrict__ values,
                        const uint16_t *__restrict__ x, void *y, int64_t rows, int64_t K)
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(256)
                 }
             }
         }
-        store_y<B, F32OUT>(y, rows, row, acc);
+        store_y<B, OUT>(y, rows, row, acc);
     }
 }
 
@@ -375,7 +375,7 @@ static nm_status encode_sparse_maps(const uint32_t *masks, const void *values, c
                      kSpCols, B, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int B, bool F32OUT>
+template <int B, int OUT>
 static nm_status launch_tma(const uint32_t *masks, const void *values, const void *x, void *y, int64_t rows,
                             int64_t K, const LaunchCtx &ctx)
 {
@@ -388,13 +388,13 @@ static nm_status launch_tma(const uint32_t *masks, const void *values, const voi
         // Few, long row blocks (at most one per SM, 64+ units each): one CTA
         // of 16 warps per row block halves each warp's share of it.
         if (nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
-            return launch_streamk<SparseUnit, B, 16, 2, 1, F32OUT>(maps, y, rows, KC, ctx);
+            return launch_streamk<SparseUnit, B, 16, 2, 1, OUT>(maps, y, rows, KC, ctx);
     }
-    return launch_streamk<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB, F32OUT>(
+    return launch_streamk<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB, OUT>(
         maps, y, rows, KC, ctx);
 }
 
-template <int B, bool F32OUT>
+template <int B, int OUT>
 static nm_status launch_simple(const uint32_t *masks, const void *values, const void *x, void *y, int64_t rows,
                                int64_t K, const LaunchCtx &ctx)
 {
@@ -409,21 +409,21 @@ static nm_status launch_simple(const uint32_t *masks, const void *values, const 
     attr[0].val.programmaticStreamSerializationAllowed = ctx.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, spmv_simple_kernel<B, F32OUT>, masks, (const uint16_t *)values,
+    if (cudaLaunchKernelEx(&cfg, spmv_simple_kernel<B, OUT>, masks, (const uint16_t *)values,
                            (const uint16_t *)x, y, rows, K) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_OK;
 }
 
-template <bool F32OUT>
+template <int OUT>
 static nm_status dispatch(const uint32_t *masks, const void *values, const void *x, void *y, int64_t rows,
                           int64_t K, int batch, const LaunchCtx &ctx)
 {
     const bool tma = spmv_path(rows, K) == kSpmvTma;
 #define NM_CASE(BB)                                                                                         \
     case BB:                                                                                                \
-        return tma ? launch_tma<BB, F32OUT>(masks, values, x, y, rows, K, ctx)                              \
-                   : launch_simple<BB, F32OUT>(masks, values, x, y, rows, K, ctx);
+        return tma ? launch_tma<BB, OUT>(masks, values, x, y, rows, K, ctx)                              \
+                   : launch_simple<BB, OUT>(masks, values, x, y, rows, K, ctx);
     switch (batch) {
         NM_CASE(1)
         NM_CASE(2)
@@ -470,11 +470,15 @@ nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t
     });
 }
 
-nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, bool f32out,
-                      int64_t rows, int64_t K, int batch, const LaunchCtx &ctx)
+nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
+                      int64_t K, int batch, const LaunchCtx &ctx)
 {
-    return f32out ? dispatch<true>(masks, values, x, y, rows, K, batch, ctx)
-                  : dispatch<false>(masks, values, x, y, rows, K, batch, ctx);
+    switch (out) {
+    case kOutBf16: return dispatch<kOutBf16>(masks, values, x, y, rows, K, batch, ctx);
+    case kOutF32: return dispatch<kOutF32>(masks, values, x, y, rows, K, batch, ctx);
+    case kOutSwiglu: return dispatch<kOutSwiglu>(masks, values, x, y, rows, K, batch, ctx);
+    default: return NM_ERR_INVALID_ARG;
+    }
 }
 
 } // namespace nm

@@ -80,14 +80,31 @@ template <class Pol, int B, int W, int NBUF> constexpr int queue_bytes()
     return B == 1 ? 16 + W * NBUF * 4 + queue_cap<W>() * 32 * 4 : 0;
 }
 
-template <int B, bool F32OUT>
+// Store row `row` (= 32 * row block + lane; all 32 lanes call this together)
+// of the output. kOutSwiglu: the rows come in gate/up pairs -- lanes 0-15 of
+// row block t hold gate rows 16t..16t+15, lanes 16-31 the up rows of the same
+// indices -- and lane i < 16 stores h[16t + i] = bf16_rn(silu(g) * u) with
+// silu(g) = g / (1 + exp(-g)), all in fp32; y is then h [batch][rows / 2].
+template <int B, int OUT>
 __device__ __forceinline__ void store_y(void *y, int64_t rows, int64_t row, const float (&v)[B])
 {
+    if constexpr (OUT == kOutSwiglu) {
+        const int lane = (int)(row & 31);
+        const int64_t hrows = rows >> 1, hr = (row >> 5) * 16 + lane;
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const float u = __shfl_down_sync(0xFFFFFFFFu, v[b], 16);
+            const float g = v[b];
+            if (lane < 16 && hr < hrows)
+                ((uint16_t *)y)[(int64_t)b * hrows + hr] = f32_to_bf16_rn(g / (1.0f + expf(-g)) * u);
+        }
+        return;
+    }
     if (row >= rows)
         return;
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-        if (F32OUT)
+        if (OUT == kOutF32)
             ((float *)y)[(int64_t)b * rows + row] = v[b];
         else
             ((uint16_t *)y)[(int64_t)b * rows + row] = f32_to_bf16_rn(v[b]);
@@ -124,7 +141,7 @@ template <int B> constexpr int part_bytes() { return 2 * B * 32 * 4; }
 // Row block rb's total over this CTA's part of it is `tot` (lanes = rows).
 // Store it, or -- when other CTAs hold parts of rb -- publish it in the scratch;
 // the CTA that publishes last adds all parts in CTA order and stores y.
-template <int B, bool F32OUT>
+template <int B, int OUT>
 __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const CtaRange &cr, int64_t rb,
                                                    const float (&tot)[B], int lane)
 {
@@ -132,7 +149,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
     const int64_t rb_lo = rb * KC, rb_hi = rb_lo + KC;
     const int64_t row = rb * kUnitRows + lane;
     if (rb_lo >= cr.cs && rb_hi <= cr.ce) {
-        store_y<B, F32OUT>(p.y, p.rows, row, tot);
+        store_y<B, OUT>(p.y, p.rows, row, tot);
         return;
     }
     const int64_t U = p.U, P = p.P;
@@ -181,7 +198,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
             for (int b = 0; b < B; ++b)
                 sum[b] += v[j][b];
     }
-    store_y<B, F32OUT>(p.y, p.rows, row, sum);
+    store_y<B, OUT>(p.y, p.rows, row, sum);
     if (lane == 0)
         atomicExch(&p.scratch.counters[first], 0u);
 }
@@ -189,7 +206,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
 // After the CTA's barrier: if this warp holds the last part of row block rb
 // inside the CTA and rb is not complete in one warp, add the CTA's parts of
 // rb (warp order, shared memory) and finish it across CTAs.
-template <int B, bool F32OUT>
+template <int B, int OUT>
 __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaRange &cr, const float *part,
                                               int64_t rb, int64_t s0, int64_t s1, int lane)
 {
@@ -216,7 +233,7 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
         for (int b = 0; b < B; ++b)
             tot[b] += q[b * 32];
     }
-    finish_across_ctas<B, F32OUT>(p, cr, rb, tot, lane);
+    finish_across_ctas<B, OUT>(p, cr, rb, tot, lane);
 }
 
 // Bytes of one warp's x ring (NBUF + 1 slots).
@@ -350,7 +367,7 @@ __device__ __forceinline__ void issue_prologue_x(const TensorMaps *maps, const W
 // of a row block in this range) that is a whole row block is stored directly;
 // other segments leave their sum in the warp's partial slot (0: the range's
 // first row block, 1: its last).
-template <class Pol, int B, int W, int NBUF, bool F32OUT>
+template <class Pol, int B, int W, int NBUF, int OUT>
 __device__ __forceinline__ void consume_range(const TensorMaps *maps, const StreamKParams &p, const WarpWork &w,
                                               uint32_t it, uint32_t stage0, const uint8_t *stage0p, uint32_t bar0,
                                               uint32_t xr0, const uint8_t *xringp, uint8_t *xfp,
@@ -410,7 +427,7 @@ __device__ __forceinline__ void consume_range(const TensorMaps *maps, const Stre
                     acc[q][b] = 0.f;
             }
             if (seg_kc0 == 0 && kc + 1 == KC) {
-                store_y<B, F32OUT>(p.y, p.rows, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
+                store_y<B, OUT>(p.y, p.rows, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
             } else {
                 float *mine = part + ((warp * 2 + (rb == w.rb0 ? 0 : 1)) * B) * 32 + lane;
 #pragma unroll
@@ -428,7 +445,7 @@ __device__ __forceinline__ void consume_range(const TensorMaps *maps, const Stre
 
 // After the CTA barrier that follows consume_range: finish the warp's first
 // and last row block (the only segments that can be partial).
-template <int B, bool F32OUT>
+template <int B, int OUT>
 __device__ __forceinline__ void finish_warp(const StreamKParams &p, const CtaRange &cr, const float *part,
                                             const WarpWork &w, int lane)
 {
@@ -436,9 +453,9 @@ __device__ __forceinline__ void finish_warp(const StreamKParams &p, const CtaRan
         return;
     const int64_t KC = p.KC;
     const int64_t rbf = w.rb0, rbl = div64(w.ue - 1, KC);
-    finish_in_cta<B, F32OUT>(p, cr, part, rbf, w.ub, rbf == rbl ? w.ue : (rbf + 1) * KC, lane);
+    finish_in_cta<B, OUT>(p, cr, part, rbf, w.ub, rbf == rbl ? w.ue : (rbf + 1) * KC, lane);
     if (rbl != rbf)
-        finish_in_cta<B, F32OUT>(p, cr, part, rbl, rbl * KC, w.ue, lane);
+        finish_in_cta<B, OUT>(p, cr, part, rbl, rbl * KC, w.ue, lane);
 }
 
 // Batch 1, a CTA range of at most queue_cap<W>() units: the warps take the
@@ -585,7 +602,7 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
 // After the CTA barrier: warp w adds the unit sums of the CTA's row blocks
 // w, w+W, ... in unit order (four interleaved partial sums, combined in a
 // fixed order) and finishes them.
-template <int B, int W, bool F32OUT>
+template <int B, int W, int OUT>
 __device__ __forceinline__ void queue_finish(const StreamKParams &p, const CtaRange &cr, QueueView qv, int warp,
                                              int lane)
 {
@@ -611,11 +628,11 @@ __device__ __forceinline__ void queue_finish(const StreamKParams &p, const CtaRa
             s4[2] += qv.upart[(u + 2) * 32 + lane];
         float tot[B];
         tot[0] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        finish_across_ctas<B, F32OUT>(p, cr, rb, tot, lane);
+        finish_across_ctas<B, OUT>(p, cr, rb, tot, lane);
     }
 }
 
-template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
+template <class Pol, int B, int W, int NBUF, int MINB, int OUT>
 __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_constant__ TensorMaps maps,
                                                                 const StreamKParams p)
 {
@@ -656,7 +673,7 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
             consume_queue<Pol, B, W, NBUF>(&maps, p, cr, qv, npre, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp,
                                            sm.pol, warp, lane, pol, pst, dead);
             __syncthreads(); // every unit sum of this CTA is in shared memory
-            queue_finish<B, W, F32OUT>(p, cr, qv, warp, lane);
+            queue_finish<B, W, OUT>(p, cr, qv, warp, lane);
             return;
         }
     }
@@ -678,11 +695,11 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
         issue_prologue_x<Pol, B, NBUF>(&maps, w, p.KC, 0, xr0, bar0);
     pdl_launch_dependents();
 
-    consume_range<Pol, B, W, NBUF, F32OUT>(&maps, p, w, 0, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp, sm.pol,
+    consume_range<Pol, B, W, NBUF, OUT>(&maps, p, w, 0, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp, sm.pol,
                                            sm.part, warp,
                                            lane, pol, pst, dead);
     __syncthreads(); // every partial of this CTA is in shared memory
-    finish_warp<B, F32OUT>(p, cr, sm.part, w, lane);
+    finish_warp<B, OUT>(p, cr, sm.part, w, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -876,12 +893,12 @@ inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
 // block. MINB CTAs of W warps share an SM, so that at a kernel boundary the
 // next kernel's CTAs can take the place of this kernel's first finishers and
 // start streaming their weights while the rest of this kernel drains.
-template <class Pol, int B, int W, int NBUF, int MINB, bool F32OUT>
+template <class Pol, int B, int W, int NBUF, int MINB, int OUT>
 nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t KC, const LaunchCtx &ctx)
 {
     constexpr int smem = streamk_smem_bytes<Pol, B, W, NBUF>();
     static_assert(MINB * (smem + 1024) <= 232448, "MINB CTAs must fit one SM's shared memory");
-    auto kern = streamk_kernel<Pol, B, W, NBUF, MINB, F32OUT>;
+    auto kern = streamk_kernel<Pol, B, W, NBUF, MINB, OUT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {

@@ -39,12 +39,20 @@ def test_header_declares_the_abi():
         assert n in names, n
 
 
+def test_linear_struct_matches_header(nm):
+    """nm_linear: five pointers, two int64, one uint32 (padded to 8 bytes)."""
+    assert ctypes.sizeof(nm.NmLinear) == 5 * 8 + 2 * 8 + 8
+    assert nm.lib().nm_abi_version() == 2
+    text = open(HEADER).read()
+    assert "uint32_t flags;" in text and "#define NM_LINEAR_SWIGLU 1u" in text
+
+
 def test_library_exports_every_declared_symbol(nm):
     L = nm.lib()
     for name in declared_functions():
         assert hasattr(L, name), f"libnmspmv.so does not export {name}"
-    assert set(declared_functions()) <= set(nm.EXPORTS) | set(declared_functions())
-    assert L.nm_abi_version() == 1
+    assert set(declared_functions()) <= set(nm.EXPORTS), set(declared_functions()) - set(nm.EXPORTS)
+    assert L.nm_abi_version() == 2
 
 
 def test_status_strings(nm):
@@ -130,6 +138,24 @@ def test_argument_validation_before_any_cuda_call(nm):
     assert h.value is None  # not set on error
     assert L.nm_stack_plan_run(None, None) == nm.NM_ERR_INVALID_ARG
     assert L.nm_stack_plan_destroy(None) == nm.NM_OK
+    # the SwiGLU pair calls: rows_h must be a multiple of 16
+    assert L.nm_spmv_swiglu(p16, p16, p16, p16, 8, 64, 1, None) == nm.NM_ERR_SHAPE
+    assert L.nm_spmv_swiglu(p16, p16, p16, p16, 16, 48, 1, None) == nm.NM_ERR_SHAPE
+    assert L.nm_spmv_swiglu(p16, p16, p16, p16, 16, 64, 9, None) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_spmv_swiglu(None, p16, p16, p16, 16, 64, 1, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_swiglu(None, None, None, None, 0, 64, 1, None) == nm.NM_OK
+    assert L.nm_pack_swiglu(p16, p16, 8, 64, 2, 4, p16, p16, None) == nm.NM_ERR_SHAPE
+    assert L.nm_pack_swiglu(p16, p16, 16, 64, 3, 4, p16, p16, None) == nm.NM_ERR_UNSUPPORTED
+    assert L.nm_pack_swiglu(p16, None, 16, 64, 2, 4, p16, p16, None) == nm.NM_ERR_INVALID_ARG
+    # a stack op's flags: unknown bits, or SwiGLU on a row count that is not a multiple of 32
+    ops[1].K = 64
+    ops[0].flags = 4
+    assert L.nm_spmv_stack(ops, 2, 1, None) == nm.NM_ERR_INVALID_ARG
+    ops[0].flags = nm.NM_LINEAR_SWIGLU
+    ops[0].rows = 16
+    assert L.nm_spmv_stack(ops, 2, 1, None) == nm.NM_ERR_SHAPE
+    ops[0].W = p16
+    assert L.dense_gemv_stack(ops, 2, 1, None) == nm.NM_ERR_INVALID_ARG
 
 
 def test_no_fallback_when_library_missing(monkeypatch):

@@ -533,5 +533,85 @@ def test_plan_falls_back_to_chained_launches(nm):
     plan.close()
 
 
+# --- gate/up SpMV with the SwiGLU epilogue ---------------------------------------------------
+
+def check_swiglu(hbf: np.ndarray, h64, g64, u64, Sg, Su, what: str):
+    """h = silu(g) * u from fp32 g, u (each within 1e-4 * S of the oracle) in fp32, rounded to bf16.
+    |silu'| <= 1.1, so |h32 - h64| <= 1.1 dg (|u| + du) + (|silu(g)| + 1.1 dg) du + 1e-6 |h|
+    (fp32 evaluation), dg = 1e-4 Sg, du = 1e-4 Su; bf16 adds one ulp."""
+    dg, du = TOL * Sg, TOL * Su
+    silu = np.abs(oracle.swiglu_f64(g64, np.ones_like(g64)))
+    bound = 1.1 * dg * (np.abs(u64) + du) + (silu + 1.1 * dg) * du + 1e-6 * np.abs(h64)
+    bound = bound + bf16_ulp(np.abs(h64) + bound)
+    err = np.abs(bits_to_f32(hbf).astype(np.float64) - h64)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{what}: {np.argwhere(bad)[:5]} err {err[bad][:5]} bound {bound[bad][:5]}"
+
+
+def swiglu_case(rows_h, K, N, M, batch, seed):
+    Wg = synth.nm_structured(rows_h, K, N, M, seed=seed)
+    Wu = synth.nm_structured(rows_h, K, N, M, seed=seed + 1)
+    x = synth.activations(batch, K, seed=seed + 2)
+    return Wg, Wu, x
+
+
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_pack_swiglu_bit_exact(nm, N, M):
+    Wg, Wu, _ = swiglu_case(48, 256, N, M, 1, seed=7)
+    masks, values = nm.pack_swiglu(Wg.cuda(), Wu.cuda(), N, M)
+    om, ov = oracle.pack(oracle.pair_rows(to_bits(Wg), to_bits(Wu)), N, M)
+    np.testing.assert_array_equal(masks_np(masks), om)
+    np.testing.assert_array_equal(to_bits(values), ov)
+
+
+# TMA path (K % 128 == 0) and fallback path; one row-block pair up to many
+@pytest.mark.parametrize("rows_h,K", [(16, 128), (48, 512), (256, 4096), (1024, 1024), (16, 96), (80, 160)])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_spmv_swiglu(nm, rows_h, K, batch):
+    Wg, Wu, x = swiglu_case(rows_h, K, 2, 4, batch, seed=rows_h + K)
+    masks, values = nm.pack_swiglu(Wg.cuda(), Wu.cuda(), 2, 4)
+    h = nm.spmv_swiglu(masks, values, x.cuda())
+    torch.cuda.synchronize()
+    h64, g64, u64, Sg, Su = oracle.spmv_swiglu_f64(to_bits(Wg), to_bits(Wu), to_bits(x))
+    check_swiglu(to_bits(h), h64, g64, u64, Sg, Su, f"swiglu {rows_h}x{K} b{batch}")
+
+
+@pytest.mark.parametrize("N,M", [(2, 4), (16, 32)])
+def test_spmv_swiglu_llama_gate_up_sampled(nm, N, M):
+    rows_h, K = synth.LLAMA31_8B["gate_up"][0] // 2, synth.LLAMA31_8B["gate_up"][1]
+    Wg = synth.nm_structured(rows_h, K, N, M, seed=21, device="cuda")
+    Wu = synth.nm_structured(rows_h, K, N, M, seed=22, device="cuda")
+    x = synth.activations(1, K, seed=23, device="cuda")
+    masks, values = nm.pack_swiglu(Wg, Wu, N, M)
+    h = nm.spmv_swiglu(masks, values, x)
+    torch.cuda.synchronize()
+    idx = sampled_rows(rows_h, 24)
+    sel = torch.from_numpy(idx).cuda()
+    h64, g64, u64, Sg, Su = oracle.spmv_swiglu_f64(to_bits(Wg[sel].cpu()), to_bits(Wu[sel].cpu()), to_bits(x.cpu()))
+    check_swiglu(to_bits(h)[:, idx], h64, g64, u64, Sg, Su, f"llama gate_up swiglu {N}:{M}")
+
+
+@pytest.mark.parametrize("persistent", [False, True])
+def test_swiglu_op_feeds_down_in_a_stack(nm, persistent):
+    """gate_up with the SwiGLU epilogue, then down reading h: an MLP of one decode layer."""
+    rows_h, K = 1024, 512
+    Wg, Wu, x = swiglu_case(rows_h, K, 2, 4, 1, seed=40)
+    Wd = synth.nm_structured(K, rows_h, 2, 4, seed=43)
+    mgu, vgu = nm.pack_swiglu(Wg.cuda(), Wu.cuda(), 2, 4)
+    md, vd = nm.pack(Wd.cuda(), 2, 4)
+    h = torch.full((1, rows_h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = torch.full((1, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ops = [dict(masks=mgu, values=vgu, x=x.cuda(), y=h, rows=2 * rows_h, K=K, flags=nm.NM_LINEAR_SWIGLU),
+           dict(masks=md, values=vd, x=h, y=y, rows=K, K=rows_h)]
+    plan = nm.StackPlan(ops, 1, persistent=persistent)  # a SwiGLU op keeps the plan on chained launches
+    plan.run()
+    torch.cuda.synchronize()
+    h64, g64, u64, Sg, Su = oracle.spmv_swiglu_f64(to_bits(Wg), to_bits(Wu), to_bits(x))
+    check_swiglu(to_bits(h), h64, g64, u64, Sg, Su, "stack swiglu")
+    y64, S = oracle.spmv_f64(to_bits(Wd), to_bits(h.cpu()))  # down on what it actually read
+    check_bf16(to_bits(y), y64, S, "stack down")
+    plan.close()
+
+
 def test_no_bounded_wait_ran_out(nm):
     assert nm.device_status() == nm.NM_OK

@@ -330,3 +330,60 @@ def test_empty_shapes():
     assert masks.shape == (0, 2) and values.shape == (0, 32)
     y, S = oracle.spmv_f64(W, np.zeros((1, 64), dtype=np.uint16))
     assert y.shape == (1, 0)
+
+
+# --- SwiGLU epilogue (the step after the gate/up SpMV) -------------------------------------------
+
+def test_swiglu_matches_scipy_expit():
+    """silu(g) * u against scipy's logistic function (a library routine), over a wide range."""
+    from scipy.special import expit
+    rng = np.random.default_rng(0)
+    g = np.concatenate([rng.normal(0, 3, 10000), np.linspace(-80, 80, 1601)])
+    u = rng.normal(0, 2, g.size)
+    h = oracle.swiglu_f64(g, u)
+    ref = expit(g) * g * u
+    np.testing.assert_allclose(h, ref, rtol=1e-13, atol=1e-300)
+
+
+def test_swiglu_closed_forms():
+    g = np.array([0.0, 1.0, -1.0, 40.0, -40.0, np.log(3.0)])
+    h = oracle.swiglu_f64(g, np.ones_like(g))
+    e = np.e
+    expect = np.array([0.0, e / (e + 1), -1 / (e + 1), 40.0 / (1 + np.exp(-40.0)), -40.0 * np.exp(-40.0) / (1 + np.exp(-40.0)),
+                       np.log(3.0) * 0.75])
+    np.testing.assert_allclose(h, expect, rtol=1e-14)
+    # linear in u, odd-even structure: silu(g) - silu(-g) = g
+    g = np.linspace(-10, 10, 101)
+    u = np.full_like(g, 2.5)
+    np.testing.assert_allclose(oracle.swiglu_f64(g, u), 2.5 * oracle.swiglu_f64(g, np.ones_like(g)), rtol=1e-15)
+    np.testing.assert_allclose(oracle.swiglu_f64(g, np.ones_like(g)) - oracle.swiglu_f64(-g, np.ones_like(g)), g,
+                               rtol=1e-13, atol=1e-13)
+    assert np.isnan(oracle.swiglu_f64(np.array([np.nan]), np.array([1.0]))[0])
+
+
+def test_pair_rows_layout():
+    rng = np.random.default_rng(1)
+    rows_h, K = 48, 64
+    Wg = rng.integers(0, 65536, (rows_h, K), dtype=np.uint16)
+    Wu = rng.integers(0, 65536, (rows_h, K), dtype=np.uint16)
+    P = oracle.pair_rows(Wg, Wu)
+    assert P.shape == (2 * rows_h, K)
+    for r in range(rows_h):
+        t, i = divmod(r, 16)
+        np.testing.assert_array_equal(P[32 * t + i], Wg[r])
+        np.testing.assert_array_equal(P[32 * t + 16 + i], Wu[r])
+    with pytest.raises(oracle.OracleError):
+        oracle.pair_rows(Wg[:40], Wu[:40])
+
+
+def test_spmv_swiglu_oracle_composes():
+    """The fused oracle equals the plain products followed by the activation."""
+    Wg = to_bits(synth.nm_structured(64, 256, 2, 4, seed=3))
+    Wu = to_bits(synth.nm_structured(64, 256, 2, 4, seed=4))
+    x = to_bits(synth.activations(2, 256, seed=5))
+    h, g, u, Sg, Su = oracle.spmv_swiglu_f64(Wg, Wu, x)
+    g2 = bits_to_f64(Wg) @ bits_to_f64(x).T
+    u2 = bits_to_f64(Wu) @ bits_to_f64(x).T
+    np.testing.assert_allclose(g, g2.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(u, u2.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h, g2.T / (1 + np.exp(-g2.T)) * u2.T, rtol=1e-12, atol=1e-15)
