@@ -186,8 +186,10 @@ class Stack:
         self.model = model
         self.layers = layers or shapes["layers"]
         self.shapes = [(name, shapes[name][0], shapes[name][1]) for name in synth.MATRICES]
+        self.patterns = list(patterns)
         self.packed = {p: [] for p in patterns}
         self.dense = []
+        self.swiglu = []  # gate_up of the first pattern in the gate/up pair layout
         for layer in range(self.layers):
             for mi, (name, rows, K) in enumerate(self.shapes):
                 W = synth.weights(rows, K, seed, synth.stream_id(CONFIG_ID, layer, mi, 0), device="cuda")
@@ -195,6 +197,8 @@ class Stack:
                 for pi, (N, M) in enumerate(patterns):
                     Wp = nm.select(W, a, N, M)
                     self.packed[(N, M)].append(nm.pack(Wp, N, M))
+                    if pi == 0 and name == "gate_up":
+                        self.swiglu.append(nm.pack_swiglu(Wp[:rows // 2], Wp[rows // 2:], N, M))
                     if keep_dense and pi == 0:
                         self.dense.append(Wp)
                     else:
@@ -232,6 +236,27 @@ class Stack:
                 continue
             m, v = self.packed[pattern][i]
             ops.append(dict(masks=m, values=v, x=xs[i], y=ys[i], rows=rows, K=K))
+        return ops
+
+    def mlp_ops(self, batch):
+        """The stack with each layer's MLP chained: gate_up with the SwiGLU epilogue writes h, and
+        down reads h as its x (qkv and o keep their own x)."""
+        _, _, xs, ys = self.io[batch]
+        ops, i = [], 0
+        for layer in range(self.layers):
+            h = None
+            for name, rows, K in self.shapes:
+                if name == "gate_up":
+                    m, v = self.swiglu[layer]
+                    h = torch.empty(batch, rows // 2, dtype=torch.bfloat16, device="cuda")
+                    ops.append(dict(masks=m, values=v, x=xs[i], y=h, rows=rows, K=K, flags=1))
+                elif name == "down":
+                    m, v = self.packed[self.patterns[0]][i]
+                    ops.append(dict(masks=m, values=v, x=h, y=ys[i], rows=rows, K=K))
+                else:
+                    m, v = self.packed[self.patterns[0]][i]
+                    ops.append(dict(masks=m, values=v, x=xs[i], y=ys[i], rows=rows, K=K))
+                i += 1
         return ops
 
     def dense_ops(self, batch):
@@ -511,6 +536,17 @@ def run_ours(args):
                 "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4)}
             del g
             pl.close()
+        # the MLP chained as in a decode layer: gate_up + SwiGLU epilogue -> h -> down
+        ops = stack.mlp_ops(B)
+        pl = nm.StackPlan(ops, B)
+        g = capture(pl.run)
+        t, _ = time_graph(g, args.steps, min(args.warmup, 10), world)
+        by = stack.bytes(B)
+        variants[f"{head[0]}:{head[1]} batch {B}, gate_up with SwiGLU epilogue feeding down"] = {
+            "us_per_token": round(t * 1e3, 2), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
+            "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4)}
+        del g
+        pl.close()
 
     # end to end through the public API: pinned host x in, stack, host y out, every step
     x_all, y_all, _, _ = stack.io[B]
