@@ -181,10 +181,64 @@ __device__ __forceinline__ bool walk_unit_b1_lut(const uint32_t (&m)[4], const u
     return true;
 }
 
-// Batch > 1: the same two-ended walk, x from the fp32 [column][batch] window.
+// x slice of one unit, bf16 [B][128] (as copied) -> bf16 [128][BP] in the
+// warp's window: the batch rows of a column side by side, two per 32-bit word.
 template <int B>
-__device__ __forceinline__ void walk_unit_bn(const uint32_t (&m)[4], const uint32_t (&v)[4][8], const uint8_t *xf, int lane,
-                                             float (&acc)[4][B])
+__device__ __forceinline__ void transpose_x_bf16(const uint8_t *sx, uint8_t *xb, int lane)
+{
+    constexpr int BP = BatchPad<B>::value;
+#pragma unroll
+    for (int i = 0; i < kSpCols / 32; ++i) {
+        const int c = lane + 32 * i;
+        uint32_t h[BP];
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+            h[b] = (b < B) ? *(const uint16_t *)(sx + b * (kSpCols * 2) + c * 2) : 0u;
+        uint8_t *dst = xb + c * BP * 2;
+        if (BP == 2) {
+            *(uint32_t *)dst = h[0] | (h[1 % BP] << 16);
+        } else if (BP == 4) {
+            *(uint2 *)dst = make_uint2(h[0] | (h[1 % BP] << 16), h[2 % BP] | (h[3 % BP] << 16));
+        } else {
+            *(uint4 *)dst = make_uint4(h[0] | (h[1 % BP] << 16), h[2 % BP] | (h[3 % BP] << 16),
+                                       h[4 % BP] | (h[5 % BP] << 16), h[6 % BP] | (h[7 % BP] << 16));
+        }
+    }
+}
+
+// acc[b] += w * x[col][b] for the batch rows: w is the WH half of `wp`, x the
+// bf16 window row at `xa`; one mixed-precision FMA per product.
+template <int B, int WH>
+__device__ __forceinline__ void fma_window_bf16(uint32_t wp, const uint8_t *xa, float (&acc)[B])
+{
+    constexpr int BP = BatchPad<B>::value;
+    uint32_t xw[BP / 2];
+    if (BP == 2) {
+        xw[0] = *(const uint32_t *)xa;
+    } else if (BP == 4) {
+        const uint2 t = *(const uint2 *)xa;
+        xw[0] = t.x;
+        xw[1 % (BP / 2)] = t.y;
+    } else {
+        const uint4 t = *(const uint4 *)xa;
+        xw[0] = t.x;
+        xw[1 % (BP / 2)] = t.y;
+        xw[2 % (BP / 2)] = t.z;
+        xw[3 % (BP / 2)] = t.w;
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        if (b & 1)
+            acc[b] = fma_bf16<WH, 1>(wp, xw[b >> 1], acc[b]);
+        else
+            acc[b] = fma_bf16<WH, 0>(wp, xw[b >> 1], acc[b]);
+    }
+}
+
+// Batch > 1: the same two-ended walk, x from the bf16 [column][batch] window.
+template <int B>
+__device__ __forceinline__ void walk_unit_bn(const uint32_t (&m)[4], const uint32_t (&v)[4][8], const uint8_t *xb,
+                                             int lane, float (&acc)[4][B])
 {
     constexpr int BP = BatchPad<B>::value;
     uint32_t mh[4], ml[4];
@@ -202,31 +256,17 @@ __device__ __forceinline__ void walk_unit_bn(const uint32_t (&m)[4], const uint3
             const uint32_t t = ml[q] - 1u;
             const int pl = bfind_u32(ml[q] ^ t);
             ml[q] &= t;
-            const int kh = 15 - j, kl = j;
-            const float wh = (kh & 1) ? bf16hi_to_f32(v[q][kh >> 1]) : bf16lo_to_f32(v[q][kh >> 1]);
-            const float wl = (kl & 1) ? bf16hi_to_f32(v[q][kl >> 1]) : bf16lo_to_f32(v[q][kl >> 1]);
-#pragma unroll
-            for (int side = 0; side < 2; ++side) {
-                const float w = side ? wl : wh;
-                const float *xa = (const float *)(xf + (q * 32 + (side ? pl : ph)) * BP * 4);
-                if (BP == 2) {
-                    const float2 xv = *(const float2 *)xa;
-                    acc[q][0] = fmaf(w, xv.x, acc[q][0]);
-                    acc[q][1 % B] = fmaf(w, xv.y, acc[q][1 % B]);
-                } else {
-#pragma unroll
-                    for (int b0 = 0; b0 < BP; b0 += 4) {
-                        if (b0 < B) {
-                            const float4 xv = *(const float4 *)(xa + b0);
-                            const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj)
-                                if (b0 + jj < B)
-                                    acc[q][(b0 + jj) % B] = fmaf(w, xs[jj], acc[q][(b0 + jj) % B]);
-                        }
-                    }
-                }
-            }
+            constexpr int kh = 15, kl = 0;
+            const uint32_t vh = v[q][(kh - j) >> 1], vl = v[q][(kl + j) >> 1];
+            const uint8_t *xh = xb + (q * 32 + ph) * BP * 2, *xl = xb + (q * 32 + pl) * BP * 2;
+            if (((kh - j) & 1) != 0)
+                fma_window_bf16<B, 1>(vh, xh, acc[q]);
+            else
+                fma_window_bf16<B, 0>(vh, xh, acc[q]);
+            if (((kl + j) & 1) != 0)
+                fma_window_bf16<B, 1>(vl, xl, acc[q]);
+            else
+                fma_window_bf16<B, 0>(vl, xl, acc[q]);
         }
     }
 }
@@ -238,7 +278,7 @@ struct SparseUnit {
     template <int B> static constexpr int stage_bytes() { return (kValBytes + kMaskBytes + 1023) / 1024 * 1024; }
     template <int B> static constexpr int x_bytes() { return 2 * kCols * B; }
     template <int B> static constexpr uint32_t tx_bytes() { return kValBytes + kMaskBytes + x_bytes<B>(); }
-    template <int B> static constexpr int xf_bytes() { return B == 1 ? 0 : kCols * BatchPad<B>::value * 4; }
+    template <int B> static constexpr int xf_bytes() { return B == 1 ? 0 : kCols * BatchPad<B>::value * 2; }
 
     static __device__ __forceinline__ void issue_weights(uint32_t st, uint32_t bar, int kc, int32_t row0,
                                                          uint64_t pol, const TensorMaps &maps)
@@ -281,7 +321,7 @@ struct SparseUnit {
             }
             walk_unit_b1(r.m, r.v, xs, lane, acc);
         } else {
-            convert_x<B, kCols>(xs, xf, lane);
+            transpose_x_bf16<B>(xs, xf, lane);
             __syncwarp();
             walk_unit_bn<B>(r.m, r.v, xf, lane, acc);
         }
