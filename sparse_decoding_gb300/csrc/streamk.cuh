@@ -68,6 +68,7 @@ struct StreamKParams {
     int32_t whole;  // CTA ranges in whole row blocks (no row block shared by CTAs)
     int32_t P;      // CTAs taking part (CTAs from P on have no work)
     int32_t shared_queue; // warps take the CTA's units from a shared counter (see consume_queue)
+    int32_t pair_k;       // CTA pairs (clusters of 2) split each row block's K in halves (see queue_finish_pair)
     uint32_t kc_inv;      // ceil(2^32 / KC): n / KC = umulhi(n, kc_inv) for the small n used
     Scratch scratch;
 };
@@ -77,7 +78,7 @@ struct StreamKParams {
 template <int W> constexpr int queue_cap() { return W >= 16 ? 128 : 96; }
 template <class Pol, int B, int W, int NBUF> constexpr int queue_bytes()
 {
-    return B == 1 ? 16 + W * NBUF * 4 + queue_cap<W>() * 32 * 4 : 0;
+    return B == 1 ? 16 + W * NBUF * 4 + queue_cap<W>() * 32 * 4 + 32 * 4 : 0;
 }
 
 // Store row `row` (= 32 * row block + lane; all 32 lanes call this together)
@@ -287,7 +288,11 @@ __device__ __forceinline__ CtaRange cta_range(const StreamKParams &p, int W, int
         cr.nw = 0;
         return cr;
     }
-    if (p.whole) {
+    if (p.pair_k) { // CTA 2t: the first half of row block t's units, CTA 2t+1 the second
+        const int64_t rb = c >> 1, h = p.KC >> 1;
+        cr.cs = rb * p.KC + ((c & 1) ? h : 0);
+        cr.ce = (c & 1) ? (rb + 1) * p.KC : rb * p.KC + h;
+    } else if (p.whole) {
         const int64_t nrb = div64(p.U, p.KC);
         cr.cs = muldiv(nrb, c, p.P) * p.KC;
         cr.ce = muldiv(nrb, c + 1, p.P) * p.KC;
@@ -471,6 +476,7 @@ struct QueueView {
     uint32_t *claim;      // next unit to hand out
     uint32_t *stage_unit; // [W][NBUF]
     float *upart;         // [cap][32]
+    float *peer;          // [32]: the other half of the row block (pair_k, rank 0)
 };
 
 template <class Pol, int B, int W, int NBUF>
@@ -480,6 +486,7 @@ __device__ __forceinline__ QueueView queue_view(uint8_t *q)
     v.claim = (uint32_t *)q;
     v.stage_unit = (uint32_t *)(q + 16);
     v.upart = (float *)(q + 16 + W * NBUF * 4);
+    v.peer = v.upart + queue_cap<W>() * 32;
     return v;
 }
 
@@ -632,6 +639,43 @@ __device__ __forceinline__ void queue_finish(const StreamKParams &p, const CtaRa
     }
 }
 
+// pair_k (batch 1): the CTA pair of a cluster holds the two halves of one
+// row block. Warp 0 of each adds its half's unit sums in unit order; rank 1
+// writes its per-row sums into rank 0's shared memory, and after the cluster
+// barrier rank 0 adds them to its own (first half + second half) and stores.
+template <int B, int W, int OUT>
+__device__ __forceinline__ void queue_finish_pair(const StreamKParams &p, const CtaRange &cr, QueueView qv, int warp,
+                                                  int lane)
+{
+    const uint32_t rank = cluster_ctarank();
+    float tot = 0.f;
+    if (warp == 0 && cr.ce > cr.cs) {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        const int64_t n = cr.ce - cr.cs;
+        int64_t u = 0;
+        for (; u + 4 <= n; u += 4) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                s4[t] += qv.upart[(u + t) * 32 + lane];
+        }
+        if (u < n)
+            s4[0] += qv.upart[u * 32 + lane];
+        if (u + 1 < n)
+            s4[1] += qv.upart[(u + 1) * 32 + lane];
+        if (u + 2 < n)
+            s4[2] += qv.upart[(u + 2) * 32 + lane];
+        tot = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        if (rank == 1)
+            st_cluster_f32(cluster_map(smem_addr(qv.peer + lane), 0), tot);
+    }
+    cluster_sync();
+    if (warp == 0 && rank == 0 && cr.ce > cr.cs) {
+        float v[B];
+        v[0] = tot + qv.peer[lane];
+        store_y<B, OUT>(p.y, p.rows, div64(cr.cs, p.KC) * kUnitRows + lane, v);
+    }
+}
+
 template <class Pol, int B, int W, int NBUF, int MINB, int OUT>
 __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_constant__ TensorMaps maps,
                                                                 const StreamKParams p)
@@ -673,7 +717,10 @@ __global__ void __launch_bounds__(W * 32, MINB) streamk_kernel(const __grid_cons
             consume_queue<Pol, B, W, NBUF>(&maps, p, cr, qv, npre, stage0, sm.stage0p, bar0, xr0, sm.xring, sm.xfp,
                                            sm.pol, warp, lane, pol, pst, dead);
             __syncthreads(); // every unit sum of this CTA is in shared memory
-            queue_finish<B, W, OUT>(p, cr, qv, warp, lane);
+            if (p.pair_k)
+                queue_finish_pair<B, W, OUT>(p, cr, qv, warp, lane);
+            else
+                queue_finish<B, W, OUT>(p, cr, qv, warp, lane);
             return;
         }
     }
@@ -728,6 +775,7 @@ __device__ __forceinline__ StreamKParams op_params(const StackOp *op, const Scra
     p.whole = op->whole;
     p.P = op->P;
     p.shared_queue = 0; // the persistent kernel splits each op statically
+    p.pair_k = 0;
     p.kc_inv = 0;
     p.scratch = scratch;
     return p;
@@ -922,17 +970,33 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     const int64_t most = sp.whole ? ((nrb + ctas - 1) / ctas) * KC : (p.U + ctas - 1) / ctas;
     p.shared_queue = (B == 1 && most <= queue_cap<W>() && KC >= 2 && KC < 32768) ? 1 : 0;
     p.kc_inv = (uint32_t)((((uint64_t)1 << 32) + KC - 1) / KC);
+    // Few row blocks (at most half the CTA slots) at batch 1: split each row
+    // block's K over a CTA pair, so that each warp's share is half as long.
+    const int64_t slots = (int64_t)ctx.num_sms * MINB;
+    p.pair_k = (B == 1 && MINB == 2 && 2 * nrb <= slots && KC % 2 == 0 && KC / 2 >= 2 && KC / 2 <= queue_cap<W>() &&
+                KC < 32768) ? 1 : 0;
+    int64_t grid = ctas;
+    if (p.pair_k) {
+        p.shared_queue = 1;
+        p.whole = 0;
+        p.P = (int32_t)(2 * nrb);
+        grid = 2 * nrb;
+    }
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(W * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = ctx.pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension; // CTA pairs (pair_k only)
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pair_k ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, maps, p) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_OK;
