@@ -127,3 +127,19 @@ MODELS = {"llama3.1-8b": LLAMA31_8B, "qwen3-14b": QWEN3_14B, "qwen3-32b": QWEN3_
           "llama3.3-70b": LLAMA33_70B}
 
 PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
+
+
+def calibration(T: int, K: int, seed: int = 0, stream: int = 5, dead=(), device="cpu") -> torch.Tensor:
+    """Calibration inputs X for one linear layer, bf16 ``[T][K]`` (token-major).
+
+    x_tj = s_j * z_tj with z ~ N(0, 1) and per-channel scales s_j ~ |N(1, 0.3^2)|,
+    every 64th channel scaled up 8x (a stand-in for the few large-magnitude
+    input channels of LLM activations). Channels listed in ``dead`` are zero in
+    every token (the case of an input that never fires)."""
+    g = _generator(seed, stream, device)
+    s = torch.randn(K, generator=g, device=device, dtype=torch.float32).mul_(0.3).add_(1.0).abs_()
+    s[::64] *= 8.0
+    if len(dead):
+        s[torch.as_tensor(list(dead), device=device)] = 0.0
+    z = torch.randn(T, K, generator=g, device=device, dtype=torch.float32)
+    return (z * s).to(torch.bfloat16)
