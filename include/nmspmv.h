@@ -59,7 +59,8 @@ typedef enum nm_status {
     NM_ERR_UNSUPPORTED = 4, /* (N, M) not a 50% pattern, batch outside 1..8 */
     NM_ERR_NOT_NM = 5,      /* an M-subgroup holds more than N nonzeros */
     NM_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
-    NM_ERR_TIMEOUT = 7      /* a kernel's bounded wait ran out */
+    NM_ERR_TIMEOUT = 7,     /* a kernel's bounded wait ran out */
+    NM_ERR_NOT_PD = 8       /* nm_obs_prune: the damped Hessian is not positive definite */
 } nm_status;
 
 /* Version of this ABI (bumped on any incompatible change). */
@@ -276,6 +277,65 @@ nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const 
  * calls that ran meanwhile are unspecified); call it before reusing the device.
  */
 nm_status nm_device_status(void *stream);
+
+/*
+ * ---- N:M pruning by the OBS rule: the step that produces the weights ----
+ *
+ * A layer is pruned against the Hessian of its calibration inputs, H = 2 X X^T
+ * (paper.rainbus.top summary, "前置知识" on the OBS framework and "方法步骤详情"
+ * step 2; ai.info summary, "Methodology in Plain English" step 1). Removing
+ * weight q costs w_q^2 / (2 [H^-1]_qq) and the remaining weights move by
+ * -(w_q / [H^-1]_qq) H^-1_{:,q}; SparseGPT applies the rule column by column.
+ * Readings where the pages stop (SparseGPT's published procedure):
+ *   - columns are fixed left to right; at column j the inverse is that of the
+ *     still-free columns, inv(H[j:, j:]);
+ *   - at the first column of every aligned M-column group, each row keeps the
+ *     N weights with the largest w_c^2 / [inv(H[c:, c:])]_00, using the values
+ *     as compensated so far; equal saliencies keep the lower column;
+ *   - damping: a zero diagonal entry (an input that is always zero) becomes 1
+ *     and its weights 0, then percdamp * mean(diag H) is added to the diagonal.
+ */
+
+/* Flag of nm_obs_prune: the lazy trailing update runs as a plain fp32 GEMM
+ * instead of fp32 emulated on the bf16 tensor cores (3 bf16 terms per operand). */
+#define NM_OBS_SGEMM 1u
+
+/*
+ * nm_obs_hessian -- H = 2 X^T X for calibration inputs X, or H += 2 X^T X.
+ *   X_bf16 : device, bf16 [T][K], one row per calibration token (read).
+ *   H      : device, fp32 [K][K], symmetric (written; accumulated into when
+ *            `accumulate` is nonzero, so long calibration sets go in chunks).
+ * Products are exact; sums are fp32. T == 0 writes zeros (or leaves H as it
+ * is when accumulating). K must be a multiple of 32; T and K at most 2^31 - 1.
+ * Asynchronous on `stream`. Calls on one device are serialized by a lock.
+ */
+nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int accumulate, void *stream);
+
+/*
+ * nm_obs_prune -- N:M pruning of one linear layer by the OBS rule above.
+ *   W_bf16      : device, bf16 [rows][K], the dense weights (read).
+ *   H           : device, fp32 [K][K], the symmetric calibration Hessian (read).
+ *   N, M        : keep N of every aligned M columns; M in {2, 4, 8, 16, 32},
+ *                 1 <= N <= M (NM_ERR_UNSUPPORTED otherwise). The decode
+ *                 format wants the 50% patterns 2:4, 4:8, 8:16, 16:32.
+ *   percdamp    : damping fraction, >= 0 and finite (0.01 is SparseGPT's).
+ *   flags       : 0 or NM_OBS_SGEMM.
+ *   W_out_bf16  : device, bf16 [rows][K] (written): the pruned weights, removed
+ *                 entries +0. This is what nm_pack / nm_pack_host take.
+ *   keep_masks  : device, uint32 [rows][K/32] or NULL (written): bit j of word g
+ *                 is set when column 32g + j is kept (the decode mask format).
+ *   W_out_f32   : device, fp32 [rows][K] or NULL: when given, it is the working
+ *                 copy during the call and ends as the pruned weights in fp32.
+ * Arithmetic is fp32 (factorisations by cuSOLVER, the trailing updates by
+ * cuBLAS, the column sweep in this library). Workspace: 8 K^2 + 4 rows K
+ * (without W_out_f32) + 512 rows bytes, taken from the stream-ordered
+ * allocator and returned before the call ends. SYNCHRONOUS: returns after the
+ * result is written (NM_ERR_NOT_PD when the damped Hessian cannot be
+ * factorised; outputs are then unspecified). Calls on one device are
+ * serialized by a lock. Pointers 16-byte aligned (NM_ERR_ALIGN).
+ */
+nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t rows, int64_t K, int N, int M, float percdamp,
+                       unsigned flags, void *W_out_bf16, uint32_t *keep_masks, float *W_out_f32, void *stream);
 
 #ifdef __cplusplus
 }

@@ -26,18 +26,20 @@ NM_ERR_UNSUPPORTED = 4
 NM_ERR_NOT_NM = 5
 NM_ERR_CUDA = 6
 NM_ERR_TIMEOUT = 7
+NM_ERR_NOT_PD = 8
 
 PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 
 NM_STACK_DENSE = 1
 NM_STACK_PERSISTENT = 2
 NM_LINEAR_SWIGLU = 1
+NM_OBS_SGEMM = 1
 
 # Every symbol the header declares (the CPU test checks they are exported).
 EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
            "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
-           "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu")
+           "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu", "nm_obs_hessian", "nm_obs_prune")
 
 
 class NmError(RuntimeError):
@@ -85,6 +87,8 @@ def lib() -> ctypes.CDLL:
         "nm_stack_plan_destroy": ([p], i32),
         "nm_pack_swiglu": ([p, p, i64, i64, i32, i32, p, p, p], i32),
         "nm_spmv_swiglu": ([p, p, p, p, i64, i64, i32, p], i32),
+        "nm_obs_hessian": ([p, i64, i64, p, i32, p], i32),
+        "nm_obs_prune": ([p, p, i64, i64, i32, i32, ctypes.c_float, ctypes.c_uint, p, p, p, p], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -299,3 +303,43 @@ class StackPlan:
             self.close()
         except Exception:
             pass
+
+
+# --- N:M pruning by the OBS rule --------------------------------------------------
+
+def obs_hessian(X: torch.Tensor, H: Optional[torch.Tensor] = None, accumulate: bool = False) -> torch.Tensor:
+    """H = 2 X^T X (or H += 2 X^T X) for calibration inputs X, bf16 [T][K] -> fp32 [K][K]."""
+    _cuda(X, torch.bfloat16, "X")
+    T, K = X.shape
+    if H is None:
+        if accumulate:
+            raise ValueError("accumulate needs H")
+        H = torch.empty(K, K, dtype=torch.float32, device=X.device)
+    _cuda(H, torch.float32, "H")
+    if tuple(H.shape) != (K, K):
+        raise ValueError("H must be [K][K]")
+    _check(lib().nm_obs_hessian(X.data_ptr(), T, K, H.data_ptr(), int(bool(accumulate)),
+                                ctypes.c_void_p(_stream(X))), "nm_obs_hessian")
+    return H
+
+
+def obs_prune(W: torch.Tensor, H: torch.Tensor, N: int, M: int, percdamp: float = 0.01, sgemm: bool = False,
+              masks: bool = True, f32: bool = False):
+    """OBS N:M pruning of W (bf16 [rows][K]) against H (fp32 [K][K]). Synchronous.
+
+    Returns (W_pruned bf16 [rows][K], keep masks int32-viewed uint32 [rows][K/32] or
+    None, W_pruned fp32 or None)."""
+    _cuda(W, torch.bfloat16, "W")
+    _cuda(H, torch.float32, "H")
+    rows, K = W.shape
+    if tuple(H.shape) != (K, K):
+        raise ValueError("H must be [K][K]")
+    out = torch.empty_like(W)
+    m = torch.empty(rows, K // 32, dtype=torch.int32, device=W.device) if masks else None
+    wf = torch.empty(rows, K, dtype=torch.float32, device=W.device) if f32 else None
+    _check(lib().nm_obs_prune(W.data_ptr(), H.data_ptr(), rows, K, N, M, float(percdamp),
+                              NM_OBS_SGEMM if sgemm else 0, out.data_ptr(),
+                              m.data_ptr() if m is not None else None,
+                              wf.data_ptr() if wf is not None else None,
+                              ctypes.c_void_p(_stream(W))), "nm_obs_prune")
+    return out, m, wf

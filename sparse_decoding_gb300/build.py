@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnmspmv.so")
 
-SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "noalloc.cu", "pack_host.cpp"]
+SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "noalloc.cu", "obs.cu", "pack_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,6 +46,13 @@ def _compile(src: str) -> tuple[str, str]:
     return obj, r.stderr
 
 
+def _rpath():
+    """Run-time search path for cuBLAS / cuSOLVER: the toolkit that nvcc belongs to."""
+    root = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
+    dirs = [d for d in (os.path.join(root, "lib64"), os.path.join(root, "lib")) if os.path.isdir(d)]
+    return [f"-Xlinker=-rpath={d}" for d in dirs]
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
@@ -65,7 +72,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for (obj, log), src in zip(results, SOURCES):
             f.write(f"==== {src}\n{log}\n")
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC"]
+    cmd = ([nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC"]
+           + ["-lcublas", "-lcusolver"] + _rpath())
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -211,7 +211,7 @@ struct nm_stack_plan {
 
 extern "C" {
 
-int nm_abi_version(void) { return 2; }
+int nm_abi_version(void) { return 3; }
 
 const char *nm_status_str(int status)
 {
@@ -224,6 +224,7 @@ const char *nm_status_str(int status)
     case NM_ERR_NOT_NM: return "an M-subgroup holds more than N nonzeros";
     case NM_ERR_CUDA: return "CUDA error";
     case NM_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
+    case NM_ERR_NOT_PD: return "the damped Hessian is not positive definite";
     default: return "unknown status";
     }
 }

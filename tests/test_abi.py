@@ -42,7 +42,7 @@ def test_header_declares_the_abi():
 def test_linear_struct_matches_header(nm):
     """nm_linear: five pointers, two int64, one uint32 (padded to 8 bytes)."""
     assert ctypes.sizeof(nm.NmLinear) == 5 * 8 + 2 * 8 + 8
-    assert nm.lib().nm_abi_version() == 2
+    assert nm.lib().nm_abi_version() == 3
     text = open(HEADER).read()
     assert "uint32_t flags;" in text and "#define NM_LINEAR_SWIGLU 1u" in text
 
@@ -52,12 +52,13 @@ def test_library_exports_every_declared_symbol(nm):
     for name in declared_functions():
         assert hasattr(L, name), f"libnmspmv.so does not export {name}"
     assert set(declared_functions()) <= set(nm.EXPORTS), set(declared_functions()) - set(nm.EXPORTS)
-    assert L.nm_abi_version() == 2
+    assert L.nm_abi_version() == 3
 
 
 def test_status_strings(nm):
-    for code in range(8):
-        assert nm.status_str(code)
+    for code in range(9):
+        assert nm.status_str(code) != "unknown status"
+    assert nm.status_str(9) == "unknown status"
     assert nm.status_str(5).startswith("an M-subgroup")
 
 
@@ -164,3 +165,37 @@ def test_no_fallback_when_library_missing(monkeypatch):
     monkeypatch.setattr(nm, "LIB_PATH", "/nonexistent/libnmspmv.so")
     with pytest.raises(RuntimeError, match="not built"):
         nm.lib()
+
+
+def test_obs_argument_validation_before_any_cuda_call(nm):
+    L = nm.lib()
+    buf = (ctypes.c_uint8 * 4096)()
+    p16 = (ctypes.addressof(buf) + 15) & ~15
+    prune = L.nm_obs_prune
+    # shape: K % 32, negative sizes
+    assert prune(p16, p16, 4, 48, 2, 4, 0.01, 0, p16, None, None, None) == nm.NM_ERR_SHAPE
+    assert prune(p16, p16, -1, 64, 2, 4, 0.01, 0, p16, None, None, None) == nm.NM_ERR_SHAPE
+    # pattern: M must divide 32, 1 <= N <= M
+    for N, M in ((2, 6), (0, 4), (5, 4), (2, 64)):
+        assert prune(p16, p16, 4, 64, N, M, 0.01, 0, p16, None, None, None) == nm.NM_ERR_UNSUPPORTED
+    # damping must be finite and >= 0; unknown flag
+    for d in (-0.1, float("nan"), float("inf")):
+        assert prune(p16, p16, 4, 64, 2, 4, d, 0, p16, None, None, None) == nm.NM_ERR_INVALID_ARG
+    assert prune(p16, p16, 4, 64, 2, 4, 0.01, 2, p16, None, None, None) == nm.NM_ERR_INVALID_ARG
+    # NULL and misaligned pointers
+    assert prune(None, p16, 4, 64, 2, 4, 0.01, 0, p16, None, None, None) == nm.NM_ERR_INVALID_ARG
+    assert prune(p16, p16, 4, 64, 2, 4, 0.01, 0, None, None, None, None) == nm.NM_ERR_INVALID_ARG
+    assert prune(p16, p16 + 4, 4, 64, 2, 4, 0.01, 0, p16, None, None, None) == nm.NM_ERR_ALIGN
+    assert prune(p16, p16, 4, 64, 2, 4, 0.01, 0, p16, p16 + 4, None, None) == nm.NM_ERR_ALIGN
+    assert prune(p16, p16, 4, 64, 2, 4, 0.01, 0, p16, None, p16 + 8, None) == nm.NM_ERR_ALIGN
+    # empty problems succeed without work
+    assert prune(None, None, 0, 64, 2, 4, 0.01, 0, None, None, None, None) == nm.NM_OK
+    assert prune(None, None, 4, 0, 2, 4, 0.01, 0, None, None, None, None) == nm.NM_OK
+    hess = L.nm_obs_hessian
+    assert hess(p16, 8, 48, p16, 0, None) == nm.NM_ERR_SHAPE
+    assert hess(p16, -1, 64, p16, 0, None) == nm.NM_ERR_SHAPE
+    assert hess(p16, 8, 64, None, 0, None) == nm.NM_ERR_INVALID_ARG
+    assert hess(None, 8, 64, p16, 0, None) == nm.NM_ERR_INVALID_ARG
+    assert hess(p16 + 2, 8, 64, p16, 0, None) == nm.NM_ERR_ALIGN
+    assert hess(None, 0, 64, p16, 1, None) == nm.NM_OK  # nothing to add
+    assert hess(None, 8, 0, None, 0, None) == nm.NM_OK
