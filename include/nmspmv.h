@@ -296,8 +296,9 @@ nm_status nm_device_status(void *stream);
  *     and its weights 0, then percdamp * mean(diag H) is added to the diagonal.
  */
 
-/* Flag of nm_obs_prune: the lazy trailing update runs as a plain fp32 GEMM
- * instead of fp32 emulated on the bf16 tensor cores (3 bf16 terms per operand). */
+/* Flag of nm_obs_prune: the factorisations and the lazy trailing updates run in
+ * plain fp32 instead of fp32 emulated on the bf16 tensor cores (each operand
+ * split into 3 bf16 terms; the default). */
 #define NM_OBS_SGEMM 1u
 
 /*
@@ -315,6 +316,7 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  * nm_obs_prune -- N:M pruning of one linear layer by the OBS rule above.
  *   W_bf16      : device, bf16 [rows][K], the dense weights (read).
  *   H           : device, fp32 [K][K], the symmetric calibration Hessian (read).
+ *                 W and H must be finite (outputs are unspecified otherwise).
  *   N, M        : keep N of every aligned M columns; M in {2, 4, 8, 16, 32},
  *                 1 <= N <= M (NM_ERR_UNSUPPORTED otherwise). The decode
  *                 format wants the 50% patterns 2:4, 4:8, 8:16, 16:32.
@@ -326,10 +328,11 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  *                 is set when column 32g + j is kept (the decode mask format).
  *   W_out_f32   : device, fp32 [rows][K] or NULL: when given, it is the working
  *                 copy during the call and ends as the pruned weights in fp32.
- * Arithmetic is fp32 (factorisations by cuSOLVER, the trailing updates by
- * cuBLAS, the column sweep in this library). Workspace: 8 K^2 + 4 rows K
- * (without W_out_f32) + 512 rows bytes, taken from the stream-ordered
- * allocator and returned before the call ends. SYNCHRONOUS: returns after the
+ * Arithmetic is fp32: the Cholesky factorisation of the reversed Hessian, its
+ * triangular inverse and the column sweep run in this library's kernels, their
+ * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K (without
+ * W_out_f32) + 4096 rows bytes, taken from the stream-ordered allocator and
+ * returned before the call ends. SYNCHRONOUS: returns after the
  * result is written (NM_ERR_NOT_PD when the damped Hessian cannot be
  * factorised; outputs are then unspecified). Calls on one device are
  * serialized by a lock. Pointers 16-byte aligned (NM_ERR_ALIGN).

@@ -47,7 +47,7 @@ def _compile(src: str) -> tuple[str, str]:
 
 
 def _rpath():
-    """Run-time search path for cuBLAS / cuSOLVER: the toolkit that nvcc belongs to."""
+    """Run-time search path for cuBLAS: the toolkit that nvcc belongs to."""
     root = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
     dirs = [d for d in (os.path.join(root, "lib64"), os.path.join(root, "lib")) if os.path.isdir(d)]
     return [f"-Xlinker=-rpath={d}" for d in dirs]
@@ -73,7 +73,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             f.write(f"==== {src}\n{log}\n")
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = ([nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC"]
-           + ["-lcublas", "-lcusolver"] + _rpath())
+           + ["-lcublas"] + _rpath())
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -13,30 +13,34 @@
 // With inv(H) = U^T U (U upper triangular), [G_j]_{0,:} / [G_j]_00 =
 // U[j, j:] / U_jj and [G_j]_00 = U_jj^2, so one factor serves every column.
 // U comes from the reversed matrix: if J reverses the index order and
-// J H J = L L^T (Cholesky), then U = J L^-1 J. That is one potrf and one
-// trtri, and inv(H) itself is never formed.
+// J H J = L L^T (Cholesky), then U = J L^-1 J. That is one Cholesky
+// factorisation and one triangular inverse; inv(H) itself is never formed.
 //
 // Steps of nm_obs_prune, all on the caller's stream:
 //   1. obs_diag_kernel: dead columns (H_jj == 0) and the damping
 //      lam = percdamp * mean(diag H with dead entries set to 1);
 //   2. obs_reverse_damp_kernel: J (H + lam I) J, dead diagonal entries = 1 + lam;
-//   3. cuSOLVER potrf (lower) and trtri (lower) on it: L^-1, column-major;
-//   4. obs_factor_kernel: U = J L^-1 J written row-major, zeros below the diagonal;
+//   3. Cholesky factorisation and inverse X = L^-1 together, by recursion on
+//      halves (chol_inv): the off-diagonal steps are GEMMs, a 128-wide
+//      diagonal block is fac_diag_kernel (one CTA factors and inverts it);
+//   4. obs_reverse_kernel: U = J X J, which for row-major X is the flat array
+//      reversed (upper triangular, zeros below the diagonal);
 //   5. obs_init_w_kernel: fp32 working copy of W, dead columns zeroed;
 //   6. per block of 128 columns [i1, i2):
 //        obs_sweep_kernel: one warp per row walks the block column by
 //          column (N:M choice, in-block compensation), writes the final
 //          values of the block, its keep bits, and the error row
 //          E[r][c] = w_c / U_cc (0 where kept);
-//        lazy trailing update W[:, i2:] -= E U[i1:i2, i2:] (cuBLAS GEMM; by
-//          default fp32 emulated on the bf16 tensor cores, 3 bf16 terms per
-//          operand, otherwise plain fp32).
+//        lazy trailing update W[:, i2:] -= E U[i1:i2, i2:], in two levels:
+//          the rest of the current 1024-column superblock after each block,
+//          every later column once per superblock (one GEMM with k = 1024).
+// Every GEMM is cuBLAS fp32: by default emulated on the bf16 tensor cores
+// (each operand split into 3 bf16 terms), with NM_OBS_SGEMM plain fp32.
 // The blocked order only regroups the same updates: a column receives every
 // earlier column's correction before it is read.
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <cusolverDn.h>
 
 #include <mutex>
 #include <vector>
@@ -47,8 +51,10 @@ namespace nm {
 namespace {
 
 constexpr int kObsBlock = 128;   // columns per sweep block
+constexpr int kSuper = 1024;     // columns per lazy-update superblock (a multiple of kObsBlock)
 constexpr int kSweepWarps = 16;  // rows in flight per CTA
 constexpr int kMaxDevices = 64;
+const float kOne = 1.0f, kMinusOne = -1.0f;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -95,29 +101,127 @@ __global__ void obs_reverse_damp_kernel(const float *__restrict__ H, int64_t K, 
     }
 }
 
-// ---- step 4: U = J L^-1 J, row-major ---------------------------------------
+// ---- step 3: the blocked Cholesky of Hr and its inverse ---------------------
 
-// Linv: column-major, lower triangle valid (element (a, b) at a + b K, a >= b).
-// U(i, j) = Linv(K-1-i, K-1-j) = Linv[K*K - 1 - (i + j K)] for j >= i, else 0.
-// A 32 x 32 tile goes through shared memory so that both sides are coalesced:
-// for a fixed j the source is contiguous in i.
-__global__ void __launch_bounds__(256) obs_factor_kernel(const float *__restrict__ Linv, int64_t K,
-                                                         float *__restrict__ U)
+constexpr int kFacB = 128;        // factorisation block
+constexpr int kFacThreads = 512;  // 4 row groups x 128 columns
+
+// One CTA factors the diagonal block [k0, k0 + kb) of the trailing-updated
+// matrix A, L_kk L_kk^T = A_kk, and writes X_kk = L_kk^-1 (lower, zeros above
+// the diagonal). L_kk itself is not stored: later steps read only blocks of L
+// below the diagonal. A block narrower than 128 is padded with the identity.
+//
+// Phase 1, the factorisation: thread t = 128 g + r holds row r, columns
+// 32 g .. 32 g + 31, of the working block in registers. Step j publishes
+// column j (one shared store per thread of group j / 32, double buffered so
+// that one barrier per step suffices), then applies a_rc -= a_rj a_cj / a_jj
+// to columns c > j. Only entries on or below the diagonal of column j are
+// read, so rows already passed may take meaningless updates; warps whose rows
+// are all passed skip the step. Column j of L (a_rj / sqrt(a_jj)) and
+// 1 / L_jj go to shared memory. A pivot that is not positive sets *not_pd and
+// is replaced by 1.
+// Phase 2, the inverse (forward substitution L X = I, right-looking): lanes
+// 4c .. 4c + 3 of the CTA hold column c of X, lane q rows 4 m + q. Step k
+// finalises X_kc = x_kc / L_kk (shuffled from its owner lane) and applies
+// x_ic -= L_ik X_kc to rows i > k. No barrier is needed: a column lives in one
+// warp. A warp skips the steps k left of its columns, where X_kc = 0.
+constexpr size_t kFacSmem = (size_t)kFacB * (kFacB + 1) * 4;
+
+__global__ void __launch_bounds__(kFacThreads, 1)
+    fac_diag_kernel(const float *__restrict__ A, float *__restrict__ X, int64_t K, int64_t k0, int kb,
+                    int *__restrict__ not_pd)
 {
-    __shared__ float t[32][33];
-    const int64_t n = K * K;
-    const int64_t i0 = (int64_t)blockIdx.y * 32, j0 = (int64_t)blockIdx.x * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-    for (int r = ty; r < 32; r += 8) {  // r: j offset, tx: i offset
-        int64_t i = i0 + tx, j = j0 + r;
-        t[r][tx] = (i < K && j < K && j >= i) ? Linv[n - 1 - (i + j * K)] : 0.0f;
+    extern __shared__ float Ls[];  // [128][129]: L_kk, row-major, padded
+    __shared__ __align__(16) float colA[2][kFacB];
+    __shared__ float rdiag[kFacB];
+    constexpr int P = kFacB + 1;
+    {
+        const int r = threadIdx.x & (kFacB - 1), g = threadIdx.x >> 7, rw0 = r & ~31;
+        float a[32];
+        if (r < kb && 32 * g < kb) {
+            const float4 *src = reinterpret_cast<const float4 *>(A + (k0 + r) * K + k0 + 32 * g);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = src[q];
+                a[4 * q] = v.x, a[4 * q + 1] = v.y, a[4 * q + 2] = v.z, a[4 * q + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < 32; ++m)
+                a[m] = (r == 32 * g + m) ? 1.0f : 0.0f;
+        }
+        bool bad = false;
+#pragma unroll 1
+        for (int gj = 0; gj < 4; ++gj) {
+#pragma unroll
+            for (int mj = 0; mj < 32; ++mj) {
+                const int j = 32 * gj + mj, buf = mj & 1;
+                if (g == gj)
+                    colA[buf][r] = a[mj];
+                __syncthreads();
+                const float d0 = colA[buf][j];
+                bad |= !(d0 > 0.0f);
+                const float rs = rsqrtf(d0 > 0.0f ? d0 : 1.0f), rd = rs * rs;
+                if (g == gj) {
+                    Ls[r * P + j] = r >= j ? a[mj] * rs : 0.0f;
+                    if (r == j)
+                        rdiag[j] = rs;
+                }
+                if (g >= gj && rw0 + 31 > j) {
+                    const float ci = colA[buf][r] * rd;
+#pragma unroll
+                    for (int m = 0; m < 32; ++m)
+                        if (g > gj || m > mj)
+                            a[m] = fmaf(-ci, colA[buf][32 * g + m], a[m]);
+                }
+            }
+        }
+        if (bad && threadIdx.x == 0)
+            atomicOr(not_pd, 1);
     }
     __syncthreads();
-    for (int r = ty; r < 32; r += 8) {  // r: i offset, tx: j offset
-        int64_t i = i0 + r, j = j0 + tx;
-        if (i < K && j < K)
-            U[i * K + j] = t[tx][r];
+    {
+        const int c = threadIdx.x >> 2, q = threadIdx.x & 3, lane = threadIdx.x & 31;
+        const int cmin = (threadIdx.x & ~31) >> 2;  // this warp's columns: cmin .. cmin + 7
+        float x[32];
+#pragma unroll
+        for (int m = 0; m < 32; ++m)
+            x[m] = (4 * m + q == c) ? 1.0f : 0.0f;
+        // k = 4 kk + kq: the register index kk is unrolled, kq is a loop
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+            if (4 * kk + 3 < cmin)
+                continue;
+#pragma unroll 1
+            for (int kq = 0; kq < 4; ++kq) {
+                const int k = 4 * kk + kq;
+                const float xk = __shfl_sync(0xffffffffu, x[kk], (lane & ~3) | kq) * rdiag[k];
+                if (q == kq)
+                    x[kk] = xk;
+                else if (q > kq)
+                    x[kk] = fmaf(-Ls[(4 * kk + q) * P + k], xk, x[kk]);
+#pragma unroll
+                for (int m = kk + 1; m < 32; ++m)
+                    x[m] = fmaf(-Ls[(4 * m + q) * P + k], xk, x[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const int i = 4 * m + q;
+            if (i < kb && c < kb)
+                X[(k0 + i) * K + k0 + c] = x[m];
+        }
     }
+}
+
+// ---- step 4: U = J X J --------------------------------------------------------
+
+// With X row-major, U(i, j) = X(K-1-i, K-1-j) = X[K*K - 1 - (i K + j)]: U is
+// the flat array of X reversed (upper triangular because X is lower).
+__global__ void obs_reverse_kernel(const float *__restrict__ X, int64_t n, float *__restrict__ U)
+{
+    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n; p += (int64_t)gridDim.x * blockDim.x)
+        U[p] = X[n - 1 - p];
 }
 
 // ---- step 5: fp32 working copy ----------------------------------------------
@@ -141,7 +245,7 @@ __global__ void obs_init_w_kernel(const __nv_bfloat16 *__restrict__ W, int64_t r
 template <int M>
 __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
     float *__restrict__ Wf, const float *__restrict__ U, int64_t rows, int64_t K, int i1, int bw, int N,
-    float *__restrict__ E, __nv_bfloat16 *__restrict__ Wout, uint32_t *__restrict__ masks)
+    float *__restrict__ E, int ldE, __nv_bfloat16 *__restrict__ Wout, uint32_t *__restrict__ masks)
 {
     extern __shared__ float4 smem4[];
     float *Ub = reinterpret_cast<float *>(smem4);
@@ -212,7 +316,7 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
                 break;
             wrow[32 * s + lane] = w[s];
             Wout[r * K + i1 + 32 * s + lane] = __float2bfloat16_rn(w[s]);
-            E[r * kObsBlock + 32 * s + lane] = e[s];
+            E[r * ldE + 32 * s + lane] = e[s];
             if (masks && lane == 0)
                 masks[r * (K / 32) + i1 / 32 + s] = keep[s];
         }
@@ -223,7 +327,7 @@ constexpr size_t kSweepSmem = (size_t)kObsBlock * kObsBlock * 4 + kObsBlock * 4;
 
 template <int M>
 cudaError_t launch_sweep(float *Wf, const float *U, int64_t rows, int64_t K, int i1, int bw, int N, float *E,
-                         __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
+                         int ldE, __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
 {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
@@ -233,19 +337,20 @@ cudaError_t launch_sweep(float *Wf, const float *U, int64_t rows, int64_t K, int
     });
     if (attr != cudaSuccess)
         return attr;
-    obs_sweep_kernel<M><<<grid, kSweepWarps * 32, kSweepSmem, st>>>(Wf, U, rows, K, i1, bw, N, E, Wout, masks);
+    obs_sweep_kernel<M><<<grid, kSweepWarps * 32, kSweepSmem, st>>>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout,
+                                                                      masks);
     return cudaGetLastError();
 }
 
 cudaError_t sweep(int M, float *Wf, const float *U, int64_t rows, int64_t K, int i1, int bw, int N, float *E,
-                  __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
+                  int ldE, __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
 {
     switch (M) {
-    case 2: return launch_sweep<2>(Wf, U, rows, K, i1, bw, N, E, Wout, masks, grid, st);
-    case 4: return launch_sweep<4>(Wf, U, rows, K, i1, bw, N, E, Wout, masks, grid, st);
-    case 8: return launch_sweep<8>(Wf, U, rows, K, i1, bw, N, E, Wout, masks, grid, st);
-    case 16: return launch_sweep<16>(Wf, U, rows, K, i1, bw, N, E, Wout, masks, grid, st);
-    default: return launch_sweep<32>(Wf, U, rows, K, i1, bw, N, E, Wout, masks, grid, st);
+    case 2: return launch_sweep<2>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
+    case 4: return launch_sweep<4>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
+    case 8: return launch_sweep<8>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
+    case 16: return launch_sweep<16>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
+    default: return launch_sweep<32>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
     }
 }
 
@@ -253,11 +358,10 @@ cudaError_t sweep(int M, float *Wf, const float *U, int64_t rows, int64_t K, int
 
 struct ObsDevice {
     cublasHandle_t blas = nullptr;
-    cusolverDnHandle_t solver = nullptr;
     int sms = 0;
 };
 
-std::mutex g_obs_mu;  // held for the whole of each call (the handles are shared)
+std::mutex g_obs_mu;  // held for the whole of each call (the handle is shared)
 ObsDevice g_obs[kMaxDevices];
 
 nm_status obs_device(ObsDevice **out)
@@ -268,13 +372,15 @@ nm_status obs_device(ObsDevice **out)
     ObsDevice &d = g_obs[dev];
     if (!d.sms && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return NM_ERR_CUDA;
-    if (!d.blas && cublasCreate(&d.blas) != CUBLAS_STATUS_SUCCESS) {
-        d.blas = nullptr;
-        return NM_ERR_CUDA;
-    }
-    if (!d.solver && cusolverDnCreate(&d.solver) != CUSOLVER_STATUS_SUCCESS) {
-        d.solver = nullptr;
-        return NM_ERR_CUDA;
+    if (!d.blas) {
+        // the inputs are finite, so the emulated GEMMs need no pass for infinities or NaN
+        if (cublasCreate(&d.blas) != CUBLAS_STATUS_SUCCESS) {
+            d.blas = nullptr;
+            return NM_ERR_CUDA;
+        }
+        if (cublasSetEmulationSpecialValuesSupport(d.blas, CUDA_EMULATION_SPECIAL_VALUES_SUPPORT_NONE) !=
+            CUBLAS_STATUS_SUCCESS)
+            return NM_ERR_CUDA;
     }
     *out = &d;
     return NM_OK;
@@ -310,6 +416,66 @@ struct Workspace {
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// Row-major fp32 GEMMs on K-strided buffers, through cuBLAS's column-major
+// interface (a row-major p x q block is the column-major q x p transpose).
+struct RowGemm {
+    cublasHandle_t h;
+    cublasComputeType_t ct;
+    int ld;
+    // C (r x c) = alpha * A (r x k) * B (k x c) + beta * C
+    bool ab(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
+    {
+        return cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, (int)c, (int)r, (int)k, &alpha, B, CUDA_R_32F, ld, A,
+                            CUDA_R_32F, ld, &beta, C, CUDA_R_32F, ld, ct, CUBLAS_GEMM_DEFAULT) ==
+               CUBLAS_STATUS_SUCCESS;
+    }
+    // C (r x c) = alpha * A (r x k) * B^T (B is c x k) + beta * C
+    bool abt(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
+    {
+        return cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)c, (int)r, (int)k, &alpha, B, CUDA_R_32F, ld, A,
+                            CUDA_R_32F, ld, &beta, C, CUDA_R_32F, ld, ct, CUBLAS_GEMM_DEFAULT) ==
+               CUBLAS_STATUS_SUCCESS;
+    }
+};
+
+// Cholesky factorisation with inverse, by recursion on halves of the block
+// range [b0, b1) (block b = columns [128 b, 128 b + 128)):
+//   [[A11, .], [A21, A22]] = L L^T,  X = L^-1:
+//     (L11, X11) from A11;  L21 = A21 X11^T;  A22 -= L21 L21^T;
+//     (L22, X22) from A22;  X21 = -X22 L21 X11.
+// A single block is fac_diag_kernel. A (J H J, damped) is destroyed; L receives
+// every block below the diagonal; X = L^-1 (its upper part must be zero on
+// entry). L21 X11 is kept in A's A21 region, which is no longer read once L21
+// exists.
+bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t b0, int64_t b1, int *not_pd,
+              cudaStream_t st)
+{
+    if (b1 - b0 == 1) {
+        const int64_t k0 = b0 * kFacB;
+        const int kb = (int)(K - k0 < kFacB ? K - k0 : kFacB);
+        static std::once_flag once;
+        static cudaError_t attr = cudaSuccess;
+        std::call_once(once, [] {
+            attr = cudaFuncSetAttribute(fac_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFacSmem);
+        });
+        if (attr != cudaSuccess)
+            return false;
+        fac_diag_kernel<<<1, kFacThreads, kFacSmem, st>>>(A, X, K, k0, kb, not_pd);
+        return cudaGetLastError() == cudaSuccess;
+    }
+    const int64_t bm = (b0 + b1) / 2;
+    const int64_t lo = b0 * kFacB, mid = bm * kFacB, hi = (b1 * kFacB < K ? b1 * kFacB : K);
+    const int64_t h1 = mid - lo, h2 = hi - mid;
+    float *A21 = A + mid * K + lo, *L21 = L + mid * K + lo;
+    float *X11 = X + lo * K + lo, *X22 = X + mid * K + mid;
+    return chol_inv(G, A, L, X, K, b0, bm, not_pd, st) &&
+           G.abt(h2, h1, h1, 1.0f, A21, X11, 0.0f, L21) &&
+           G.abt(h2, h2, h1, -1.0f, L21, L21, 1.0f, A + mid * K + mid) &&
+           chol_inv(G, A, L, X, K, bm, b1, not_pd, st) &&
+           G.ab(h2, h1, h1, 1.0f, L21, X11, 0.0f, A21) &&
+           G.ab(h2, h1, h2, -1.0f, X22, A21, 0.0f, X + mid * K + lo);
+}
+
 nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K, int N, int M, float percdamp,
                          unsigned flags, void *Wout, uint32_t *masks, float *Wout_f32, cudaStream_t st)
 {
@@ -317,81 +483,72 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     nm_status s = obs_device(&d);
     if (s != NM_OK)
         return s;
-    if (cublasSetStream(d->blas, st) != CUBLAS_STATUS_SUCCESS ||
-        cusolverDnSetStream(d->solver, st) != CUSOLVER_STATUS_SUCCESS)
+    if (cublasSetStream(d->blas, st) != CUBLAS_STATUS_SUCCESS)
         return NM_ERR_CUDA;
+    const bool plain = (flags & NM_OBS_SGEMM) != 0;
+    const RowGemm G{d->blas, plain ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_EMULATED_16BFX9, (int)K};
 
-    // buffers: dead flags, lam, solver info, the factor (in place), U, E, the fp32 working copy
+    // buffers: dead flags, lam, the not-PD flag, three K x K matrices, E, the fp32 working copy
     const size_t kk = (size_t)K * K * 4;
-    const size_t off_lam = round256((size_t)K), off_info = off_lam + 256, off_L = off_info + 256;
-    const size_t off_U = off_L + round256(kk), off_E = off_U + round256(kk);
-    const size_t off_Wf = off_E + round256((size_t)rows * kObsBlock * 4);
+    const size_t off_lam = round256((size_t)K), off_flag = off_lam + 256, off_A = off_flag + 256;
+    const size_t off_L = off_A + round256(kk), off_X = off_L + round256(kk), off_E = off_X + round256(kk);
+    const size_t off_Wf = off_E + round256((size_t)rows * kSuper * 4);
     const size_t total = off_Wf + (Wout_f32 ? 0 : round256((size_t)rows * K * 4));
-    Workspace ws(st), solver_ws(st);
+    Workspace ws(st);
     if (!ws.alloc(total))
         return NM_ERR_CUDA;
     char *base = (char *)ws.p;
     unsigned char *dead = (unsigned char *)base;
     float *lam = (float *)(base + off_lam);
-    int *info = (int *)(base + off_info);
-    float *L = (float *)(base + off_L), *U = (float *)(base + off_U), *E = (float *)(base + off_E);
+    int *not_pd = (int *)(base + off_flag);
+    float *A = (float *)(base + off_A), *L = (float *)(base + off_L), *X = (float *)(base + off_X);
+    float *E = (float *)(base + off_E);
     float *Wf = Wout_f32 ? Wout_f32 : (float *)(base + off_Wf);
+    float *U = L;  // U replaces L once X is complete
 
-    const int n = (int)K;
-    int lwork = 0;
-    size_t trtri_dev = 0, trtri_host = 0;
-    if (cusolverDnSpotrf_bufferSize(d->solver, CUBLAS_FILL_MODE_LOWER, n, L, n, &lwork) != CUSOLVER_STATUS_SUCCESS ||
-        cusolverDnXtrtri_bufferSize(d->solver, CUBLAS_FILL_MODE_LOWER, CUBLAS_DIAG_NON_UNIT, K, CUDA_R_32F, L, K,
-                                    &trtri_dev, &trtri_host) != CUSOLVER_STATUS_SUCCESS)
-        return NM_ERR_CUDA;
-    const size_t off_tw = round256((size_t)lwork * 4);
-    if (!solver_ws.alloc(off_tw + round256(trtri_dev) + 256))
-        return NM_ERR_CUDA;
-    float *pw = (float *)solver_ws.p;
-    void *tw = (char *)solver_ws.p + off_tw;
-    std::vector<char> host_work(trtri_host ? trtri_host : 1);
-
-    if (cudaMemsetAsync(info, 0, 2 * sizeof(int), st) != cudaSuccess)
+    if (cudaMemsetAsync(not_pd, 0, sizeof(int), st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess)
         return NM_ERR_CUDA;
     obs_diag_kernel<<<1, 1024, 0, st>>>(H, K, percdamp, dead, lam);
-    obs_reverse_damp_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(H, K, lam, L);
+    obs_reverse_damp_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(H, K, lam, A);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
-    if (cusolverDnSpotrf(d->solver, CUBLAS_FILL_MODE_LOWER, n, L, n, pw, lwork, info) != CUSOLVER_STATUS_SUCCESS ||
-        cusolverDnXtrtri(d->solver, CUBLAS_FILL_MODE_LOWER, CUBLAS_DIAG_NON_UNIT, K, CUDA_R_32F, L, K, tw, trtri_dev,
-                         host_work.data(), trtri_host, info + 1) != CUSOLVER_STATUS_SUCCESS)
+    if (!chol_inv(G, A, L, X, K, 0, (K + kFacB - 1) / kFacB, not_pd, st))
         return NM_ERR_CUDA;
-    int hinfo[2] = {0, 0};
-    if (cudaMemcpyAsync(hinfo, info, sizeof(hinfo), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+    int host_flag = 0;
+    if (cudaMemcpyAsync(&host_flag, not_pd, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
-    if (hinfo[0] != 0 || hinfo[1] != 0)
+    if (host_flag)
         return NM_ERR_NOT_PD;
-
-    const dim3 tiles((unsigned)((K + 31) / 32), (unsigned)((K + 31) / 32));
-    obs_factor_kernel<<<tiles, 256, 0, st>>>(L, K, U);
+    obs_reverse_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(X, K * K, U);
     obs_init_w_kernel<<<grid_for(rows * K, d->sms), 256, 0, st>>>((const __nv_bfloat16 *)W, rows, K, dead, Wf);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
 
     const int64_t want = (rows + kSweepWarps - 1) / kSweepWarps, cap = (int64_t)d->sms * 3;
     const int sweep_grid = (int)(want < cap ? want : cap);
-    const cublasComputeType_t ct =
-        (flags & NM_OBS_SGEMM) ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_EMULATED_16BFX9;
-    const float alpha = -1.0f, beta = 1.0f;
-    for (int64_t i1 = 0; i1 < K; i1 += kObsBlock) {
-        const int bw = (int)(K - i1 < kObsBlock ? K - i1 : kObsBlock);
-        const int64_t i2 = i1 + bw;
-        if (sweep(M, Wf, U, rows, K, (int)i1, bw, N, E, (__nv_bfloat16 *)Wout, masks, sweep_grid, st) !=
-            cudaSuccess)
-            return NM_ERR_CUDA;
-        if (i2 < K) {
-            // column-major view: (W[:, i2:])^T -= (U[i1:i2, i2:])^T E^T
-            if (cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_N, (int)(K - i2), (int)rows, bw, &alpha,
-                             U + i1 * K + i2, CUDA_R_32F, n, E, CUDA_R_32F, kObsBlock, &beta, Wf + i2, CUDA_R_32F, n,
-                             ct, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    // Two-level lazy update: inside a superblock of kSuper columns each swept
+    // block updates the rest of the superblock (k = 128); at the end of the
+    // superblock one GEMM with k = kSuper updates every later column.
+    auto update = [&](int64_t c0, int64_t c1, int64_t k0, int64_t kw, const float *Ek) {
+        // W[:, c0:c1] -= E[:, k0 - s1 ...] U[k0:k0+kw, c0:c1]   (E rows have stride kSuper)
+        return cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_N, (int)(c1 - c0), (int)rows, (int)kw, &kMinusOne,
+                            U + k0 * K + c0, CUDA_R_32F, (int)K, Ek, CUDA_R_32F, kSuper, &kOne, Wf + c0, CUDA_R_32F,
+                            (int)K, G.ct, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+    };
+    for (int64_t s1 = 0; s1 < K; s1 += kSuper) {
+        const int64_t s2 = (s1 + kSuper < K ? s1 + kSuper : K);
+        for (int64_t i1 = s1; i1 < s2; i1 += kObsBlock) {
+            const int bw = (int)(s2 - i1 < kObsBlock ? s2 - i1 : kObsBlock);
+            const int64_t i2 = i1 + bw;
+            if (sweep(M, Wf, U, rows, K, (int)i1, bw, N, E + (i1 - s1), kSuper, (__nv_bfloat16 *)Wout, masks,
+                      sweep_grid, st) != cudaSuccess)
+                return NM_ERR_CUDA;
+            if (i2 < s2 && !update(i2, s2, i1, bw, E + (i1 - s1)))
                 return NM_ERR_CUDA;
         }
+        if (s2 < K && !update(s2, K, s1, s2 - s1, E))
+            return NM_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
