@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (0 = the model's)")
     ap.add_argument("--no-variants", action="store_true", help="skip the extra pattern/batch lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pruning", action="store_true", help="skip the OBS pruning measurement")
     return ap.parse_args()
 
 
@@ -451,6 +452,72 @@ def workload_config(model, N, M, batch, layers):
             "launch": "CUDA graph of PDL-chained launches (a prepared nm_stack_plan)"}
 
 
+def obs_flops(rows, K):
+    """Algorithmic fp32 flops of OBS N:M pruning of one 50% linear: Cholesky
+    factorisation K^3/3 and triangular inverse K^3/3 of the (reversed) Hessian,
+    and the compensations, 2 (K - 1 - j) flops for each of the rows K / 2
+    removed weights, rows K^2 / 2 in all."""
+    return 2 * K ** 3 / 3 + rows * K ** 2 / 2
+
+
+def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True):
+    """Prune one decoder layer by the OBS rule and pack it: for each linear the
+    calibration Hessian H = 2 X^T X of its own synthetic inputs, the pruning,
+    and the bitmask pack. nm_obs_prune is synchronous, so event and wall time
+    agree; each linear takes the best of `repeats` after one untimed run."""
+    shapes = [(n, synth.MODELS[model][n]) for n in synth.MATRICES]
+    per, hess_ms, total_flops = {}, 0.0, 0.0
+    for mi, (name, (rows, K)) in enumerate(shapes):
+        W = synth.weights(rows, K, seed=7, stream=synth.stream_id(9, 0, mi, 0), device="cuda")
+        X = synth.calibration(tokens, K, seed=7, stream=synth.stream_id(9, 0, mi, 3), device="cuda")
+        H = nm.obs_hessian(X)
+        best = None
+        for it in range(repeats + 1):
+            torch.cuda.synchronize()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+            nm.obs_hessian(X, H)
+            e[1].record()
+            Wp, _, _ = nm.obs_prune(W, H, N, M, masks=False)
+            e[2].record()
+            masks, values = nm.pack(Wp, N, M)
+            e[3].record()
+            torch.cuda.synchronize()
+            t = [e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+            if it > 0 and (best is None or sum(t) < sum(best)):
+                best = t
+        f = obs_flops(rows, K)
+        total_flops += f
+        hess_ms += best[0]
+        per[name] = {"rows": rows, "K": K, "hessian_ms": round(best[0], 3), "prune_ms": round(best[1], 3),
+                     "pack_ms": round(best[2], 3),
+                     "fp32_tflops_effective": round(f / (best[1] * 1e-3) / 1e12, 2)}
+        del W, X, H, Wp, masks, values
+    total_ms = sum(v["hessian_ms"] + v["prune_ms"] + v["pack_ms"] for v in per.values())
+    out = {"workload": f"one {model} decoder layer pruned {N}:{M} by the OBS rule, each linear against the "
+                       f"Hessian of {tokens} synthetic calibration tokens, then packed",
+           "ms_per_layer": round(total_ms, 2), "hessian_ms": round(hess_ms, 3),
+           "fp32_tflops_effective": round(total_flops / (sum(v["prune_ms"] for v in per.values()) * 1e-3) / 1e12, 2),
+           "algorithmic_flops": f"{total_flops:.4g} (2 K^3 / 3 + rows K^2 / 2 per linear)",
+           "per_linear": per}
+    if cpu:
+        sys.path.insert(0, ROOT)
+        from oracle import obs
+        rows, K = synth.MODELS[model]["o"]
+        Wc = synth.weights(64, K, seed=7).float().numpy().astype("float64")
+        Xc = _bits(synth.calibration(tokens, K, seed=7))
+        t0 = time.perf_counter()
+        Hc = obs.hessian_f64(Xc)
+        t1 = time.perf_counter()
+        obs.obs_prune_f64(Wc, Hc, N, M)
+        t2 = time.perf_counter()
+        out["cpu_oracle"] = {"hessian_s": round(t1 - t0, 2), "prune_s": round(t2 - t1, 2),
+                             "sample": f"o linear ({rows}x{K}): 64 of its {rows} rows, fp64 numpy "
+                                       f"(factorisation of the whole {K}x{K} Hessian included)",
+                             "cores": cpu_cores_available()}
+    return out
+
+
 def run_ours(args):
     rank, world, local = dist_init()
     torch.cuda.set_device(local)
@@ -548,6 +615,10 @@ def run_ours(args):
         del g
         pl.close()
 
+    pruning = None
+    if world == 1 and not args.no_pruning:
+        pruning = run_obs_pruning(nm, args.model, N, M, cpu=(world == 1 and not args.no_cpu_baseline))
+
     # end to end through the public API: pinned host x in, stack, host y out, every step
     x_all, y_all, _, _ = stack.io[B]
     x_host = torch.empty(x_all.shape, dtype=x_all.dtype, pin_memory=True)
@@ -595,6 +666,7 @@ def run_ours(args):
                                        "over the event-timed step (gaps between launches included)"},
         "per_shape": per_shape,
         "variants": variants,
+        "obs_pruning": pruning,
         "e2e": {"value": round(job_us_per_token(e2e_ms, world), 3), "unit": UNIT,
                 "h2d_bytes_per_step": x_all.numel() * 2, "d2h_bytes_per_step": y_all.numel() * 2,
                 "path": "pinned host x -> device, nm_stack_plan_run through the C ABI (no graph), y -> pinned host"},
