@@ -518,6 +518,39 @@ def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True):
     return out
 
 
+def splitk_compare(nm, stack, pattern, world, steps, warmup):
+    """The two ways to combine a row block split over CTAs, fp32 output: the
+    default deterministic fix-up (the last CTA adds the parts in CTA order) and
+    the split reduction with atomicAdd (every CTA of the layer's split adds its
+    part into the zeroed y). Each timing runs the layers' own weights of one
+    shape in one graph."""
+    out = {}
+    for name in ("o", "down"):
+        idx = [i for i, (n, _, _) in enumerate(stack.linears()) if n == name]
+        rows, K = synth.MODELS[stack.model][name]
+        for b in (1, 8):
+            xs = [synth.activations(b, K, 3, synth.stream_id(CONFIG_ID, li, 9, 2), device="cuda")
+                  for li in range(len(idx))]
+            ys = [torch.empty(b, rows, dtype=torch.float32, device="cuda") for _ in idx]
+            res = {}
+            for atomic in (False, True):
+                def run(atomic=atomic):
+                    for j, i in enumerate(idx):
+                        m, v = stack.packed[pattern][i]
+                        nm.spmv(m, v, xs[j], out=ys[j], f32=True, atomic=atomic)
+                g = capture(run)
+                t, _ = time_graph(g, steps, warmup, world)
+                res["atomic" if atomic else "deterministic"] = t * 1e3 / len(idx)
+                del g
+            by = sparse_bytes(rows, K, b)
+            out[f"{name} {rows}x{K} batch {b}"] = {
+                "deterministic_us": round(res["deterministic"], 3), "atomic_us": round(res["atomic"], 3),
+                "deterministic_GB_s": round(by / (res["deterministic"] * 1e-6) / 1e9, 1),
+                "atomic_GB_s": round(by / (res["atomic"] * 1e-6) / 1e9, 1)}
+            del xs, ys
+    return out
+
+
 def run_ours(args):
     rank, world, local = dist_init()
     torch.cuda.set_device(local)
@@ -615,6 +648,10 @@ def run_ours(args):
         del g
         pl.close()
 
+    split_k = None
+    if not args.no_variants:
+        split_k = splitk_compare(nm, stack, head, world, max(5, args.steps // 2), min(args.warmup, 5))
+
     pruning = None
     if world == 1 and not args.no_pruning:
         pruning = run_obs_pruning(nm, args.model, N, M, cpu=(world == 1 and not args.no_cpu_baseline))
@@ -666,6 +703,7 @@ def run_ours(args):
                                        "over the event-timed step (gaps between launches included)"},
         "per_shape": per_shape,
         "variants": variants,
+        "split_k_combine": split_k,
         "obs_pruning": pruning,
         "e2e": {"value": round(job_us_per_token(e2e_ms, world), 3), "unit": UNIT,
                 "h2d_bytes_per_step": x_all.numel() * 2, "d2h_bytes_per_step": y_all.numel() * 2,

@@ -130,6 +130,22 @@ nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const v
                          float *y_f32, int64_t rows, int64_t K, int batch, void *stream);
 
 /*
+ * nm_spmv_f32out_atomic -- nm_spmv_f32out computed as a split reduction with
+ * atomicAdd (paper.rainbus.top summary, "方法步骤详情" step 4, where the
+ * decode kernel splits a reduction and combines it with atomicAdd when
+ * needed). The K range of every row block is split over all CTA slots of the
+ * device (at least 8 units of 32 rows x 256 columns each); the CTAs that
+ * share a row block add their partial sums into y with fp32 atomicAdd after
+ * the call has zeroed y on `stream`. Arguments, layouts and errors are those
+ * of nm_spmv_f32out; the result obeys the same error bound, but the order of
+ * the additions (and so the last bits) may change from call to call.
+ * nm_spmv_f32out's default combine is the deterministic one: the last CTA to
+ * finish a shared row block adds all parts in CTA order.
+ */
+nm_status nm_spmv_f32out_atomic(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
+                                int64_t rows, int64_t K, int batch, void *stream);
+
+/*
  * dense_gemv -- the dense bf16 reference on the same GPU (the pages' 1.00x
  * baseline: aitest123.com article, Table 3; ai.info summary, Main Findings).
  *   W_bf16: device bf16 [rows][K]; x_bf16: device bf16 [batch][K];

@@ -39,7 +39,8 @@ NM_OBS_SGEMM = 1
 EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_pack", "nm_spmv",
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
            "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
-           "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu", "nm_obs_hessian", "nm_obs_prune")
+           "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu", "nm_obs_hessian", "nm_obs_prune",
+           "nm_spmv_f32out_atomic")
 
 
 class NmError(RuntimeError):
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
         "nm_pack": ([p, i64, i64, i32, i32, p, p, p], i32),
         "nm_spmv": ([p, p, p, p, i64, i64, i32, p], i32),
         "nm_spmv_f32out": ([p, p, p, p, i64, i64, i32, p], i32),
+        "nm_spmv_f32out_atomic": ([p, p, p, p, i64, i64, i32, p], i32),
         "dense_gemv": ([p, p, p, i64, i64, i32, p], i32),
         "dense_gemv_f32out": ([p, p, p, i64, i64, i32, p], i32),
         "nm_spmv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
@@ -173,8 +175,13 @@ def pack_host(W: torch.Tensor, N: int, M: int):
 
 
 def spmv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, out: Optional[torch.Tensor] = None,
-         f32: bool = False) -> torch.Tensor:
-    """y[b][r] = sum_j W[r][j] x[b][j] over the bitmask format; bf16 (or fp32 with f32=True)."""
+         f32: bool = False, atomic: bool = False) -> torch.Tensor:
+    """y[b][r] = sum_j W[r][j] x[b][j] over the bitmask format; bf16 (or fp32 with f32=True).
+
+    atomic=True (fp32 only): the split-K variant that combines row-block parts
+    with atomicAdd (nm_spmv_f32out_atomic)."""
+    if atomic and not f32:
+        raise ValueError("the atomicAdd split-K variant writes fp32 (f32=True)")
     _cuda(masks, torch.int32, "masks")
     _cuda(values, torch.bfloat16, "values")
     x = _cuda(_x2d(x), torch.bfloat16, "x")
@@ -185,9 +192,9 @@ def spmv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, out: Option
         raise ValueError("shape mismatch between masks, values and x")
     odt = torch.float32 if f32 else torch.bfloat16
     out = torch.empty(batch, rows, dtype=odt, device=x.device) if out is None else _cuda(out, odt, "out")
-    fn = lib().nm_spmv_f32out if f32 else lib().nm_spmv
-    _check(fn(masks.data_ptr(), values.data_ptr(), x.data_ptr(), out.data_ptr(), rows, K, batch,
-              ctypes.c_void_p(_stream(x))), "nm_spmv_f32out" if f32 else "nm_spmv")
+    name = "nm_spmv_f32out_atomic" if atomic else "nm_spmv_f32out" if f32 else "nm_spmv"
+    _check(getattr(lib(), name)(masks.data_ptr(), values.data_ptr(), x.data_ptr(), out.data_ptr(), rows, K, batch,
+                                ctypes.c_void_p(_stream(x))), name)
     return out
 
 

@@ -120,7 +120,7 @@ static nm_status zero_output(void *y, int64_t rows, int batch, size_t elt, cudaS
 
 // out: kOutBf16, kOutF32, or kOutSwiglu (rows = gate/up pair rows, y = h [batch][rows / 2]).
 static nm_status spmv_impl(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
-                           int64_t K, int batch, cudaStream_t stream, bool pdl)
+                           int64_t K, int batch, cudaStream_t stream, bool pdl, bool splitk_atomic = false)
 {
     nm_status s = check_spmv_args(masks, values, x, y, rows, K, batch);
     if (s != NM_OK || rows == 0)
@@ -133,6 +133,7 @@ static nm_status spmv_impl(const uint32_t *masks, const void *values, const void
     LaunchCtx ctx;
     if ((s = device_ctx(stream, pdl, &ctx)) != NM_OK)
         return s;
+    ctx.splitk_atomic = splitk_atomic;
     s = launch_spmv(masks, values, x, y, out, rows, K, batch, ctx);
     if (s == NM_OK && cudaGetLastError() != cudaSuccess)
         s = NM_ERR_CUDA;
@@ -284,6 +285,12 @@ nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const v
                          int64_t rows, int64_t K, int batch, void *stream)
 {
     return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false);
+}
+
+nm_status nm_spmv_f32out_atomic(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
+                                int64_t rows, int64_t K, int batch, void *stream)
+{
+    return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false, true);
 }
 
 nm_status dense_gemv(const void *W_bf16, const void *x_bf16, void *y_bf16, int64_t rows, int64_t K, int batch,

@@ -15,6 +15,9 @@ struct LaunchCtx {
     bool pdl;        // launch with programmatic stream serialization
     Scratch scratch; // per-device scratch
     int num_sms;
+    // Split K over every CTA slot and add the parts of a shared row block with
+    // fp32 atomicAdd into y (fp32 output only; the launcher zeroes y first).
+    bool splitk_atomic = false;
 };
 
 // Which kernel nm_spmv uses for a shape (exposed for tests and tooling).

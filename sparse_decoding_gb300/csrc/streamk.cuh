@@ -70,6 +70,7 @@ struct StreamKParams {
     int32_t shared_queue; // warps take the CTA's units from a shared counter (see consume_queue)
     int32_t pair_k;       // CTA pairs (clusters of 2) split each row block's K in halves (see queue_finish_pair)
     uint32_t kc_inv;      // ceil(2^32 / KC): n / KC = umulhi(n, kc_inv) for the small n used
+    int32_t atomic;       // parts of a shared row block go to y by fp32 atomicAdd (y zeroed before)
     Scratch scratch;
 };
 
@@ -141,7 +142,9 @@ template <int B> constexpr int part_bytes() { return 2 * B * 32 * 4; }
 
 // Row block rb's total over this CTA's part of it is `tot` (lanes = rows).
 // Store it, or -- when other CTAs hold parts of rb -- publish it in the scratch;
-// the CTA that publishes last adds all parts in CTA order and stores y.
+// the CTA that publishes last adds all parts in CTA order and stores y. In the
+// atomic variant (fp32 output) each part is added into the zeroed y instead:
+// the split reduction with atomicAdd; the order of the adds is not fixed.
 template <int B, int OUT>
 __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const CtaRange &cr, int64_t rb,
                                                    const float (&tot)[B], int lane)
@@ -152,6 +155,16 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
     if (rb_lo >= cr.cs && rb_hi <= cr.ce) {
         store_y<B, OUT>(p.y, p.rows, row, tot);
         return;
+    }
+    if constexpr (OUT == kOutF32) {
+        if (p.atomic) {
+            if (row < p.rows) {
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+                    atomicAdd((float *)p.y + (int64_t)b * p.rows + row, tot[b]);
+            }
+            return;
+        }
     }
     const int64_t U = p.U, P = p.P;
     const int64_t c = blockIdx.x;
@@ -777,6 +790,7 @@ __device__ __forceinline__ StreamKParams op_params(const StackOp *op, const Scra
     p.shared_queue = 0; // the persistent kernel splits each op statically
     p.pair_k = 0;
     p.kc_inv = 0;
+    p.atomic = 0;
     p.scratch = scratch;
     return p;
 }
@@ -981,6 +995,20 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
         p.whole = 0;
         p.P = (int32_t)(2 * nrb);
         grid = 2 * nrb;
+    }
+    p.atomic = 0;
+    if (OUT == kOutF32 && ctx.splitk_atomic) {
+        // Split K over every CTA slot (at least kMinUnitsPerCta units each);
+        // the parts of a shared row block meet in y by atomicAdd.
+        const int64_t P = std::max<int64_t>(1, std::min<int64_t>(slots, p.U / kMinUnitsPerCta));
+        p.atomic = 1;
+        p.whole = 0;
+        p.pair_k = 0;
+        p.P = (int32_t)P;
+        grid = P;
+        p.shared_queue = (B == 1 && (p.U + P - 1) / P <= queue_cap<W>() && KC >= 2 && KC < 32768) ? 1 : 0;
+        if (cudaMemsetAsync(y, 0, (size_t)rows * B * 4, ctx.stream) != cudaSuccess)
+            return NM_ERR_CUDA;
     }
 
     cudaLaunchConfig_t cfg = {};
