@@ -58,6 +58,10 @@ def parse_args():
     ap.add_argument("--no-variants", action="store_true", help="skip the extra pattern/batch lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pruning", action="store_true", help="skip the OBS pruning measurement")
+    ap.add_argument("--only-pruning", action="store_true",
+                    help="run only the OBS pruning measurement and print its JSON object")
+    ap.add_argument("--prune-linears", default="qkv,o,gate_up,down", help="linears to prune (comma list)")
+    ap.add_argument("--prune-repeats", type=int, default=2, help="timed repeats per linear (after one untimed)")
     return ap.parse_args()
 
 
@@ -460,14 +464,14 @@ def obs_flops(rows, K):
     return 2 * K ** 3 / 3 + rows * K ** 2 / 2
 
 
-def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True):
+def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True, linears=synth.MATRICES):
     """Prune one decoder layer by the OBS rule and pack it: for each linear the
     calibration Hessian H = 2 X^T X of its own synthetic inputs, the pruning,
     and the bitmask pack. nm_obs_prune is synchronous, so event and wall time
     agree; each linear takes the best of `repeats` after one untimed run."""
-    shapes = [(n, synth.MODELS[model][n]) for n in synth.MATRICES]
+    shapes = [(mi, n, synth.MODELS[model][n]) for mi, n in enumerate(synth.MATRICES) if n in linears]
     per, hess_ms, total_flops = {}, 0.0, 0.0
-    for mi, (name, (rows, K)) in enumerate(shapes):
+    for mi, name, (rows, K) in shapes:
         W = synth.weights(rows, K, seed=7, stream=synth.stream_id(9, 0, mi, 0), device="cuda")
         X = synth.calibration(tokens, K, seed=7, stream=synth.stream_id(9, 0, mi, 3), device="cuda")
         H = nm.obs_hessian(X)
@@ -494,7 +498,8 @@ def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True):
                      "fp32_tflops_effective": round(f / (best[1] * 1e-3) / 1e12, 2)}
         del W, X, H, Wp, masks, values
     total_ms = sum(v["hessian_ms"] + v["prune_ms"] + v["pack_ms"] for v in per.values())
-    out = {"workload": f"one {model} decoder layer pruned {N}:{M} by the OBS rule, each linear against the "
+    out = {"workload": f"{'one ' + model + ' decoder layer' if len(per) == 4 else model + ' ' + ', '.join(per)} "
+                       f"pruned {N}:{M} by the OBS rule, each linear against the "
                        f"Hessian of {tokens} synthetic calibration tokens, then packed",
            "ms_per_layer": round(total_ms, 2), "hessian_ms": round(hess_ms, 3),
            "fp32_tflops_effective": round(total_flops / (sum(v["prune_ms"] for v in per.values()) * 1e-3) / 1e12, 2),
@@ -738,6 +743,15 @@ def run_ours(args):
 
 def main():
     args = parse_args()
+    if args.only_pruning:
+        import sparse_decoding_gb300 as nm
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        nm.init()
+        N, M = parse_pattern(args.pattern)
+        out = run_obs_pruning(nm, args.model, N, M, repeats=args.prune_repeats, cpu=not args.no_cpu_baseline,
+                              linears=tuple(args.prune_linears.split(",")))
+        print(json.dumps({"obs_pruning": out}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
