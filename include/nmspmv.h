@@ -342,12 +342,11 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  *                 entries +0. This is what nm_pack / nm_pack_host take.
  *   keep_masks  : device, uint32 [rows][K/32] or NULL (written): bit j of word g
  *                 is set when column 32g + j is kept (the decode mask format).
- *   W_out_f32   : device, fp32 [rows][K] or NULL: when given, it is the working
- *                 copy during the call and ends as the pruned weights in fp32.
+ *   W_out_f32   : device, fp32 [rows][K] or NULL (written): the pruned weights
+ *                 in fp32, before the rounding to bf16.
  * Arithmetic is fp32: the Cholesky factorisation of the reversed Hessian, its
  * triangular inverse and the column sweep run in this library's kernels, their
- * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K (without
- * W_out_f32) + 4096 rows bytes, taken from the stream-ordered allocator and
+ * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K + 4096 rows bytes, taken from the stream-ordered allocator and
  * returned before the call ends. SYNCHRONOUS: returns after the
  * result is written (NM_ERR_NOT_PD when the damped Hessian cannot be
  * factorised; outputs are then unspecified). Calls on one device are

@@ -13,31 +13,31 @@
 // With inv(H) = U^T U (U upper triangular), [G_j]_{0,:} / [G_j]_00 =
 // U[j, j:] / U_jj and [G_j]_00 = U_jj^2, so one factor serves every column.
 // U comes from the reversed matrix: if J reverses the index order and
-// J H J = L L^T (Cholesky), then U = J L^-1 J. That is one Cholesky
-// factorisation and one triangular inverse; inv(H) itself is never formed.
+// J H J = L L^T (Cholesky), then H = R R^T with R = J L J upper triangular
+// and U = R^-1 = J L^-1 J. The sweep needs only U's 128 x 128 diagonal blocks
+// (the inverses of L's diagonal blocks); the corrections between blocks are
+// carried by R itself: with E the errors (w_j / U_jj for removed weights, 0
+// for kept ones) and D = W0 - final weights, D = E U, so E = D R, and what the
+// finished blocks owe block b is -(D R)_b U_bb.
 //
 // Steps of nm_obs_prune, all on the caller's stream:
 //   1. obs_diag_kernel: dead columns (H_jj == 0) and the damping
 //      lam = percdamp * mean(diag H with dead entries set to 1);
-//   2. obs_reverse_damp_kernel: J (H + lam I) J, dead diagonal entries = 1 + lam;
-//   3. Cholesky factorisation and inverse X = L^-1 together, by recursion on
-//      halves (chol_inv): the off-diagonal steps are GEMMs, a 128-wide
-//      diagonal block is fac_diag_kernel (one CTA factors and inverts it);
-//   4. obs_reverse_kernel: U = J X J, which for row-major X is the flat array
-//      reversed (upper triangular, zeros below the diagonal);
-//   5. obs_init_w_kernel: fp32 working copy of W, dead columns zeroed;
-//   6. per block of 128 columns [i1, i2):
-//        obs_sweep_kernel: one warp per row walks the block column by
-//          column (N:M choice, in-block compensation), writes the final
-//          values of the block, its keep bits, and the error row
-//          E[r][c] = w_c / U_cc (0 where kept);
-//        lazy trailing update W[:, i2:] -= E U[i1:i2, i2:], in two levels:
-//          the rest of the current 1024-column superblock after each block,
-//          every later column once per superblock (one GEMM with k = 1024).
+//      obs_reverse_damp_kernel: J (H + lam I) J, dead diagonal entries 1 + lam;
+//   2. chol_inv: the Cholesky factorisation L by recursion on halves; the
+//      off-diagonal steps are GEMMs, and a 128-wide diagonal block is
+//      fac_diag_kernel (one CTA factors it and inverts it). Only the inverses
+//      that the recursion itself needs are formed in full;
+//   3. obs_reverse_kernel: R = J L J (L's flat array reversed);
+//   4. per block (128 columns; a narrower one first), obs_sweep_kernel: one
+//      warp per row starts from W0 + P U_bb and walks the block column by
+//      column (N:M choice, in-block compensation); it writes the block's final
+//      values, keep bits and D;
+//   5. the lazy update P += D R, in two levels: the rest of the current
+//      1024-column superblock after each block, every later column once per
+//      superblock (one GEMM with k up to 1024).
 // Every GEMM is cuBLAS fp32: by default emulated on the bf16 tensor cores
 // (each operand split into 3 bf16 terms), with NM_OBS_SGEMM plain fp32.
-// The blocked order only regroups the same updates: a column receives every
-// earlier column's correction before it is read.
 #include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -214,49 +214,46 @@ __global__ void __launch_bounds__(kFacThreads, 1)
     }
 }
 
-// ---- step 4: U = J X J --------------------------------------------------------
+// ---- step 4: R = J L J ----------------------------------------------------------
 
-// With X row-major, U(i, j) = X(K-1-i, K-1-j) = X[K*K - 1 - (i K + j)]: U is
-// the flat array of X reversed (upper triangular because X is lower).
-__global__ void obs_reverse_kernel(const float *__restrict__ X, int64_t n, float *__restrict__ U)
+// With L row-major, R(i, j) = L(K-1-i, K-1-j) = L[K*K - 1 - (i K + j)]: R is
+// the flat array of L reversed; H + lam I = R R^T with R upper triangular.
+__global__ void obs_reverse_kernel(const float *__restrict__ L, int64_t n, float *__restrict__ R)
 {
     for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n; p += (int64_t)gridDim.x * blockDim.x)
-        U[p] = X[n - 1 - p];
-}
-
-// ---- step 5: fp32 working copy ----------------------------------------------
-
-__global__ void obs_init_w_kernel(const __nv_bfloat16 *__restrict__ W, int64_t rows, int64_t K,
-                                  const unsigned char *__restrict__ dead, float *__restrict__ Wf)
-{
-    const int64_t n = rows * K;
-    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n; p += (int64_t)gridDim.x * blockDim.x)
-        Wf[p] = dead[p % K] ? 0.0f : __bfloat162float(W[p]);
+        R[p] = L[n - 1 - p];
 }
 
 // ---- step 6a: the column sweep of one block ----------------------------------
 
-// Shared memory: Ub[a][b] = U[i1 + a][i1 + b] for a, b < bw (zeros below the
-// diagonal and outside the block) and rinv[a] = 1 / Ub[a][a].
+// One block [i1, i1 + bw) of columns, all rows. Shared memory:
+// Ub[a][c] = U[i1 + a][i1 + c] = X[K-1-i1-a][K-1-i1-c] (U = J X J; zeros below
+// the diagonal and outside the block) and rinv[a] = 1 / Ub[a][a].
 // Warp w of CTA c takes rows c * 16 + w, then steps by the grid. Lane l holds
-// columns i1 + 32 s + l (s = 0..3) in w[s]. A kept column moves nothing, so
-// only removed columns run the update; the below-diagonal zeros of Ub leave
-// the already final columns of the slot unchanged.
+// columns i1 + 32 s + l (s = 0..3).
+//   start : w = W0 + P U_bb, with W0 the dense weights (dead columns 0) and P
+//           the accumulated D R of the blocks to the left (see the host side);
+//   sweep : at the first column of each M-group the lanes of the group rank
+//           their saliencies w^2 / U_cc^2 (equal ones by column) and keep the
+//           N largest; a removed column j sends err = w_j / U_jj and every
+//           later column c of the block takes w_c -= err U_jc (kept columns
+//           move nothing; the zeros of Ub below the diagonal leave the passed
+//           columns as they are);
+//   output: the final values (bf16, and fp32 if asked), the keep bits as the
+//           decode format's mask words, and D = W0 - final.
 template <int M>
-__global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
-    float *__restrict__ Wf, const float *__restrict__ U, int64_t rows, int64_t K, int i1, int bw, int N,
-    float *__restrict__ E, int ldE, __nv_bfloat16 *__restrict__ Wout, uint32_t *__restrict__ masks)
+__global__ void __launch_bounds__(kSweepWarps * 32, 2) obs_sweep_kernel(
+    const __nv_bfloat16 *__restrict__ W, const unsigned char *__restrict__ dead, const float *__restrict__ P,
+    const float *__restrict__ X, int64_t rows, int64_t K, int i1, int bw, int N, float *__restrict__ D, int ldD,
+    __nv_bfloat16 *__restrict__ Wout, float *__restrict__ Wout_f32, uint32_t *__restrict__ masks)
 {
     extern __shared__ float4 smem4[];
     float *Ub = reinterpret_cast<float *>(smem4);
     float *rinv = Ub + kObsBlock * kObsBlock;
-    constexpr int kQuads = kObsBlock / 4;
-    for (int q = threadIdx.x; q < kObsBlock * kQuads; q += blockDim.x) {
-        const int a = q / kQuads, b = (q % kQuads) * 4;
-        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (a < bw && b < bw)
-            v = *reinterpret_cast<const float4 *>(U + (int64_t)(i1 + a) * K + i1 + b);
-        smem4[q] = v;
+    const int64_t last = K * K - 1;
+    for (int q = threadIdx.x; q < kObsBlock * kObsBlock; q += blockDim.x) {
+        const int a = q / kObsBlock, c = q % kObsBlock;
+        Ub[q] = (a < bw && c < bw && c >= a) ? X[last - ((int64_t)(i1 + a) * K + i1 + c)] : 0.0f;
     }
     __syncthreads();
     for (int a = threadIdx.x; a < kObsBlock; a += blockDim.x)
@@ -266,14 +263,30 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = bw >> 5;
     for (int64_t r = (int64_t)blockIdx.x * kSweepWarps + warp; r < rows; r += (int64_t)gridDim.x * kSweepWarps) {
-        float *wrow = Wf + r * K + i1;
-        float w[4], e[4];
+        const int64_t base = r * K + i1;
+        float w0[4], w[4], p[4];
         uint32_t keep[4];
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-            w[s] = s < ns ? wrow[32 * s + lane] : 0.0f;
-            e[s] = 0.0f;
+            const int64_t col = i1 + 32 * s + lane;
+            w0[s] = (s < ns && !dead[col]) ? __bfloat162float(W[base + 32 * s + lane]) : 0.0f;
+            p[s] = s < ns ? P[base + 32 * s + lane] : 0.0f;
+            w[s] = w0[s];
             keep[s] = 0u;
+        }
+        // w += p U_bb  (row a of Ub holds zeros left of its diagonal)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            if (s >= ns)
+                break;
+#pragma unroll 4
+            for (int l = 0; l < 32; ++l) {
+                const float pa = __shfl_sync(0xffffffffu, p[s], l);
+                const float *urow = Ub + (32 * s + l) * kObsBlock;
+#pragma unroll
+                for (int s2 = s; s2 < 4; ++s2)
+                    w[s2] = fmaf(pa, urow[32 * s2 + lane], w[s2]);
+            }
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
@@ -283,19 +296,16 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
             for (int l = 0; l < 32; ++l) {
                 const int i = 32 * s + l;
                 if ((l & (M - 1)) == 0) {
-                    // N:M choice for the group starting at column i, from the
-                    // current values: rank by saliency w^2 / U_cc^2, equal
-                    // saliencies ranked by column.
                     const float d = Ub[(32 * s + lane) * kObsBlock + 32 * s + lane];
                     const float sc = w[s] * w[s] / (d * d);
-                    const int base = lane & ~(M - 1);
+                    const int grp = lane & ~(M - 1);
                     int rank = 0;
 #pragma unroll
                     for (int t = 0; t < M; ++t) {
-                        const float o = __shfl_sync(0xffffffffu, sc, base + t);
-                        rank += (o > sc) || (o == sc && base + t < lane);
+                        const float o = __shfl_sync(0xffffffffu, sc, grp + t);
+                        rank += (o > sc) || (o == sc && grp + t < lane);
                     }
-                    keep[s] |= __ballot_sync(0xffffffffu, base == l && rank < N);
+                    keep[s] |= __ballot_sync(0xffffffffu, grp == l && rank < N);
                 }
                 if (!((keep[s] >> l) & 1u)) {
                     const float err = __shfl_sync(0xffffffffu, w[s], l) * rinv[i];
@@ -303,10 +313,8 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
 #pragma unroll
                     for (int s2 = s; s2 < 4; ++s2)
                         w[s2] = fmaf(-err, urow[32 * s2 + lane], w[s2]);
-                    if (lane == l) {
+                    if (lane == l)
                         w[s] = 0.0f;
-                        e[s] = err;
-                    }
                 }
             }
         }
@@ -314,9 +322,10 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
         for (int s = 0; s < 4; ++s) {
             if (s >= ns)
                 break;
-            wrow[32 * s + lane] = w[s];
-            Wout[r * K + i1 + 32 * s + lane] = __float2bfloat16_rn(w[s]);
-            E[r * ldE + 32 * s + lane] = e[s];
+            Wout[base + 32 * s + lane] = __float2bfloat16_rn(w[s]);
+            if (Wout_f32)
+                Wout_f32[base + 32 * s + lane] = w[s];
+            D[r * ldD + 32 * s + lane] = w0[s] - w[s];
             if (masks && lane == 0)
                 masks[r * (K / 32) + i1 / 32 + s] = keep[s];
         }
@@ -325,9 +334,20 @@ __global__ void __launch_bounds__(kSweepWarps * 32) obs_sweep_kernel(
 
 constexpr size_t kSweepSmem = (size_t)kObsBlock * kObsBlock * 4 + kObsBlock * 4;
 
-template <int M>
-cudaError_t launch_sweep(float *Wf, const float *U, int64_t rows, int64_t K, int i1, int bw, int N, float *E,
-                         int ldE, __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
+struct SweepArgs {
+    const __nv_bfloat16 *W;
+    const unsigned char *dead;
+    const float *P, *X;
+    int64_t rows, K;
+    int N;
+    float *D;
+    int ldD;
+    __nv_bfloat16 *Wout;
+    float *Wout_f32;
+    uint32_t *masks;
+};
+
+template <int M> cudaError_t launch_sweep(const SweepArgs &a, int i1, int bw, int grid, cudaStream_t st)
 {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
@@ -337,20 +357,19 @@ cudaError_t launch_sweep(float *Wf, const float *U, int64_t rows, int64_t K, int
     });
     if (attr != cudaSuccess)
         return attr;
-    obs_sweep_kernel<M><<<grid, kSweepWarps * 32, kSweepSmem, st>>>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout,
-                                                                      masks);
+    obs_sweep_kernel<M><<<grid, kSweepWarps * 32, kSweepSmem, st>>>(a.W, a.dead, a.P, a.X, a.rows, a.K, i1, bw, a.N,
+                                                                      a.D, a.ldD, a.Wout, a.Wout_f32, a.masks);
     return cudaGetLastError();
 }
 
-cudaError_t sweep(int M, float *Wf, const float *U, int64_t rows, int64_t K, int i1, int bw, int N, float *E,
-                  int ldE, __nv_bfloat16 *Wout, uint32_t *masks, int grid, cudaStream_t st)
+cudaError_t sweep(int M, const SweepArgs &a, int i1, int bw, int grid, cudaStream_t st)
 {
     switch (M) {
-    case 2: return launch_sweep<2>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
-    case 4: return launch_sweep<4>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
-    case 8: return launch_sweep<8>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
-    case 16: return launch_sweep<16>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
-    default: return launch_sweep<32>(Wf, U, rows, K, i1, bw, N, E, ldE, Wout, masks, grid, st);
+    case 2: return launch_sweep<2>(a, i1, bw, grid, st);
+    case 4: return launch_sweep<4>(a, i1, bw, grid, st);
+    case 8: return launch_sweep<8>(a, i1, bw, grid, st);
+    case 16: return launch_sweep<16>(a, i1, bw, grid, st);
+    default: return launch_sweep<32>(a, i1, bw, grid, st);
     }
 }
 
@@ -438,17 +457,20 @@ struct RowGemm {
     }
 };
 
-// Cholesky factorisation with inverse, by recursion on halves of the block
-// range [b0, b1) (block b = columns [128 b, 128 b + 128)):
-//   [[A11, .], [A21, A22]] = L L^T,  X = L^-1:
-//     (L11, X11) from A11;  L21 = A21 X11^T;  A22 -= L21 L21^T;
-//     (L22, X22) from A22;  X21 = -X22 L21 X11.
-// A single block is fac_diag_kernel. A (J H J, damped) is destroyed; L receives
-// every block below the diagonal; X = L^-1 (its upper part must be zero on
-// entry). L21 X11 is kept in A's A21 region, which is no longer read once L21
-// exists.
-bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t b0, int64_t b1, int *not_pd,
-              cudaStream_t st)
+// Cholesky factorisation, by recursion on halves of the block range [b0, b1)
+// (block b = columns [128 b, 128 b + 128)):
+//   [[A11, .], [A21, A22]] = L L^T:
+//     L11 and X11 = L11^-1 from A11;  L21 = A21 X11^T;  A22 -= L21 L21^T;
+//     L22 from A22;  and, if need_x, X21 = -X22 L21 X11 so that X = L^-1 in full.
+// The left half is always inverted in full (its inverse makes L21); below the
+// top call only nodes whose own inverse some L21 needs invert in full. A
+// single block is fac_diag_kernel, which also writes X_kk = L_kk^-1: the
+// diagonal blocks of X are always complete. A (J H J, damped) is destroyed; L
+// receives every block below the diagonal (its diagonal blocks are not
+// written); X's upper part must be zero on entry. L21 X11 is kept in A's A21
+// region, which is no longer read once L21 exists.
+bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t b0, int64_t b1, bool need_x,
+              int *not_pd, cudaStream_t st)
 {
     if (b1 - b0 == 1) {
         const int64_t k0 = b0 * kFacB;
@@ -468,12 +490,21 @@ bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t
     const int64_t h1 = mid - lo, h2 = hi - mid;
     float *A21 = A + mid * K + lo, *L21 = L + mid * K + lo;
     float *X11 = X + lo * K + lo, *X22 = X + mid * K + mid;
-    return chol_inv(G, A, L, X, K, b0, bm, not_pd, st) &&
-           G.abt(h2, h1, h1, 1.0f, A21, X11, 0.0f, L21) &&
-           G.abt(h2, h2, h1, -1.0f, L21, L21, 1.0f, A + mid * K + mid) &&
-           chol_inv(G, A, L, X, K, bm, b1, not_pd, st) &&
-           G.ab(h2, h1, h1, 1.0f, L21, X11, 0.0f, A21) &&
-           G.ab(h2, h1, h2, -1.0f, X22, A21, 0.0f, X + mid * K + lo);
+    if (!chol_inv(G, A, L, X, K, b0, bm, true, not_pd, st) || !G.abt(h2, h1, h1, 1.0f, A21, X11, 0.0f, L21) ||
+        !G.abt(h2, h2, h1, -1.0f, L21, L21, 1.0f, A + mid * K + mid) ||
+        !chol_inv(G, A, L, X, K, bm, b1, need_x, not_pd, st))
+        return false;
+    if (!need_x)
+        return true;
+    return G.ab(h2, h1, h1, 1.0f, L21, X11, 0.0f, A21) && G.ab(h2, h1, h2, -1.0f, X22, A21, 0.0f, X + mid * K + lo);
+}
+
+// The sweep's blocks in column order: the factorisation's blocks reversed, so
+// a block narrower than 128 (K % 128 != 0) comes first.
+int64_t sweep_bound(int64_t b, int64_t nb, int64_t K)
+{
+    const int64_t first = K - (int64_t)kObsBlock * (nb - 1);
+    return b == 0 ? 0 : (b >= nb ? K : first + (int64_t)kObsBlock * (b - 1));
 }
 
 nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K, int N, int M, float percdamp,
@@ -488,12 +519,13 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     const bool plain = (flags & NM_OBS_SGEMM) != 0;
     const RowGemm G{d->blas, plain ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_EMULATED_16BFX9, (int)K};
 
-    // buffers: dead flags, lam, the not-PD flag, three K x K matrices, E, the fp32 working copy
+    // buffers: dead flags, lam, the not-PD flag, three K x K matrices (A, later
+    // R; L; X), D of one superblock, the accumulator P
     const size_t kk = (size_t)K * K * 4;
     const size_t off_lam = round256((size_t)K), off_flag = off_lam + 256, off_A = off_flag + 256;
-    const size_t off_L = off_A + round256(kk), off_X = off_L + round256(kk), off_E = off_X + round256(kk);
-    const size_t off_Wf = off_E + round256((size_t)rows * kSuper * 4);
-    const size_t total = off_Wf + (Wout_f32 ? 0 : round256((size_t)rows * K * 4));
+    const size_t off_L = off_A + round256(kk), off_X = off_L + round256(kk), off_D = off_X + round256(kk);
+    const size_t off_P = off_D + round256((size_t)rows * kSuper * 4);
+    const size_t total = off_P + round256((size_t)rows * K * 4);
     Workspace ws(st);
     if (!ws.alloc(total))
         return NM_ERR_CUDA;
@@ -502,17 +534,18 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     float *lam = (float *)(base + off_lam);
     int *not_pd = (int *)(base + off_flag);
     float *A = (float *)(base + off_A), *L = (float *)(base + off_L), *X = (float *)(base + off_X);
-    float *E = (float *)(base + off_E);
-    float *Wf = Wout_f32 ? Wout_f32 : (float *)(base + off_Wf);
-    float *U = L;  // U replaces L once X is complete
+    float *Dbuf = (float *)(base + off_D), *P = (float *)(base + off_P);
+    float *R = A;  // R replaces A once the factorisation is done
 
-    if (cudaMemsetAsync(not_pd, 0, sizeof(int), st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess)
+    if (cudaMemsetAsync(not_pd, 0, sizeof(int), st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess ||
+        cudaMemsetAsync(P, 0, (size_t)rows * K * 4, st) != cudaSuccess)
         return NM_ERR_CUDA;
     obs_diag_kernel<<<1, 1024, 0, st>>>(H, K, percdamp, dead, lam);
     obs_reverse_damp_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(H, K, lam, A);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
-    if (!chol_inv(G, A, L, X, K, 0, (K + kFacB - 1) / kFacB, not_pd, st))
+    const int64_t nb = (K + kFacB - 1) / kFacB;
+    if (!chol_inv(G, A, L, X, K, 0, nb, false, not_pd, st))
         return NM_ERR_CUDA;
     int host_flag = 0;
     if (cudaMemcpyAsync(&host_flag, not_pd, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -520,34 +553,40 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
         return NM_ERR_CUDA;
     if (host_flag)
         return NM_ERR_NOT_PD;
-    obs_reverse_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(X, K * K, U);
-    obs_init_w_kernel<<<grid_for(rows * K, d->sms), 256, 0, st>>>((const __nv_bfloat16 *)W, rows, K, dead, Wf);
+    obs_reverse_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(L, K * K, R);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
 
-    const int64_t want = (rows + kSweepWarps - 1) / kSweepWarps, cap = (int64_t)d->sms * 3;
+    // Sweep the blocks left to right. A block starts from W0 + P U_bb, where P
+    // accumulates D R over the finished blocks (D = W0 - final values): with
+    // E the errors, W0 - final = E U and U = R^-1, so E = D R, and the
+    // corrections the finished blocks owe block b, sum E_c U_cb, equal
+    // -(D R)_b U_bb. P is updated lazily in two levels: after each block the
+    // rest of its superblock (k = block width), after each superblock every
+    // later column (k = superblock width).
+    const int64_t want = (rows + kSweepWarps - 1) / kSweepWarps, cap = (int64_t)d->sms * 2;
     const int sweep_grid = (int)(want < cap ? want : cap);
-    // Two-level lazy update: inside a superblock of kSuper columns each swept
-    // block updates the rest of the superblock (k = 128); at the end of the
-    // superblock one GEMM with k = kSuper updates every later column.
-    auto update = [&](int64_t c0, int64_t c1, int64_t k0, int64_t kw, const float *Ek) {
-        // W[:, c0:c1] -= E[:, k0 - s1 ...] U[k0:k0+kw, c0:c1]   (E rows have stride kSuper)
-        return cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_N, (int)(c1 - c0), (int)rows, (int)kw, &kMinusOne,
-                            U + k0 * K + c0, CUDA_R_32F, (int)K, Ek, CUDA_R_32F, kSuper, &kOne, Wf + c0, CUDA_R_32F,
+    const SweepArgs sa{(const __nv_bfloat16 *)W, dead, P, X, rows, K, N, Dbuf, kSuper, (__nv_bfloat16 *)Wout,
+                       Wout_f32, masks};
+    auto update = [&](int64_t c0, int64_t c1, int64_t k0, int64_t kw, const float *Dk) {
+        // P[:, c0:c1] += D[:, k0 ...] R[k0:k0+kw, c0:c1]   (D rows have stride kSuper)
+        return cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_N, (int)(c1 - c0), (int)rows, (int)kw, &kOne,
+                            R + k0 * K + c0, CUDA_R_32F, (int)K, Dk, CUDA_R_32F, kSuper, &kOne, P + c0, CUDA_R_32F,
                             (int)K, G.ct, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
     };
-    for (int64_t s1 = 0; s1 < K; s1 += kSuper) {
-        const int64_t s2 = (s1 + kSuper < K ? s1 + kSuper : K);
-        for (int64_t i1 = s1; i1 < s2; i1 += kObsBlock) {
-            const int bw = (int)(s2 - i1 < kObsBlock ? s2 - i1 : kObsBlock);
-            const int64_t i2 = i1 + bw;
-            if (sweep(M, Wf, U, rows, K, (int)i1, bw, N, E + (i1 - s1), kSuper, (__nv_bfloat16 *)Wout, masks,
-                      sweep_grid, st) != cudaSuccess)
+    constexpr int64_t kPerSuper = kSuper / kObsBlock;
+    for (int64_t sb = 0; sb < nb; sb += kPerSuper) {
+        const int64_t s1 = sweep_bound(sb, nb, K), s2 = sweep_bound(sb + kPerSuper, nb, K);
+        for (int64_t b = sb; b < sb + kPerSuper && b < nb; ++b) {
+            const int64_t i1 = sweep_bound(b, nb, K), i2 = sweep_bound(b + 1, nb, K);
+            SweepArgs a = sa;
+            a.D = Dbuf + (i1 - s1);
+            if (sweep(M, a, (int)i1, (int)(i2 - i1), sweep_grid, st) != cudaSuccess)
                 return NM_ERR_CUDA;
-            if (i2 < s2 && !update(i2, s2, i1, bw, E + (i1 - s1)))
+            if (i2 < s2 && !update(i2, s2, i1, i2 - i1, Dbuf + (i1 - s1)))
                 return NM_ERR_CUDA;
         }
-        if (s2 < K && !update(s2, K, s1, s2 - s1, E))
+        if (s2 < K && !update(s2, K, s1, s2 - s1, Dbuf))
             return NM_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
