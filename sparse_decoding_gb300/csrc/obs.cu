@@ -226,18 +226,30 @@ __global__ void obs_reverse_kernel(const float *__restrict__ L, int64_t n, float
 
 // ---- step 6a: the column sweep of one block ----------------------------------
 
+// Bits 0..7 of x moved to bits 0, 4, 8, ..., 28.
+__device__ __forceinline__ uint32_t spread8(uint32_t x)
+{
+    x &= 0xFFu;
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;
+    return x;
+}
+
 // One block [i1, i1 + bw) of columns, all rows. Shared memory:
 // Ub[a][c] = U[i1 + a][i1 + c] = X[K-1-i1-a][K-1-i1-c] (U = J X J; zeros below
-// the diagonal and outside the block) and rinv[a] = 1 / Ub[a][a].
+// the diagonal and outside the block), rinv[a] = 1 / Ub[a][a] and
+// dsq[a] = rinv[a]^2.
 // Warp w of CTA c takes rows c * 16 + w, then steps by the grid. Lane l holds
-// columns i1 + 32 s + l (s = 0..3).
+// columns i1 + 4 l + t (t = 0..3), so a row of Ub is one 16-byte load per lane
+// and a 2- or 4-column group lies in one lane.
 //   start : w = W0 + P U_bb, with W0 the dense weights (dead columns 0) and P
 //           the accumulated D R of the blocks to the left (see the host side);
-//   sweep : at the first column of each M-group the lanes of the group rank
-//           their saliencies w^2 / U_cc^2 (equal ones by column) and keep the
-//           N largest; a removed column j sends err = w_j / U_jj and every
-//           later column c of the block takes w_c -= err U_jc (kept columns
-//           move nothing; the zeros of Ub below the diagonal leave the passed
+//   sweep : at the first column of each M-group the group ranks its
+//           saliencies w^2 / U_cc^2 (equal ones by column) and keeps the N
+//           largest; a removed column j sends err = w_j / U_jj and every later
+//           column c of the block takes w_c -= err U_jc (kept columns move
+//           nothing; the zeros of Ub below the diagonal leave the passed
 //           columns as they are);
 //   output: the final values (bf16, and fp32 if asked), the keep bits as the
 //           decode format's mask words, and D = W0 - final.
@@ -250,89 +262,148 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) obs_sweep_kernel(
     extern __shared__ float4 smem4[];
     float *Ub = reinterpret_cast<float *>(smem4);
     float *rinv = Ub + kObsBlock * kObsBlock;
-    const int64_t last = K * K - 1;
-    for (int q = threadIdx.x; q < kObsBlock * kObsBlock; q += blockDim.x) {
-        const int a = q / kObsBlock, c = q % kObsBlock;
-        Ub[q] = (a < bw && c < bw && c >= a) ? X[last - ((int64_t)(i1 + a) * K + i1 + c)] : 0.0f;
+    float *dsq = rinv + kObsBlock;
+    constexpr int kQuads = kObsBlock / 4;
+    for (int q = threadIdx.x; q < kObsBlock * kQuads; q += blockDim.x) {
+        const int a = q / kQuads, c = (q % kQuads) * 4;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (a < bw && c < bw) {
+            // columns K-4-i1-c .. K-1-i1-c of row K-1-i1-a, reversed
+            const float4 x = *reinterpret_cast<const float4 *>(X + (K - 1 - i1 - a) * K + (K - 4 - i1 - c));
+            v = make_float4(c >= a ? x.w : 0.0f, c + 1 >= a ? x.z : 0.0f, c + 2 >= a ? x.y : 0.0f,
+                            c + 3 >= a ? x.x : 0.0f);
+        }
+        smem4[q] = v;
     }
     __syncthreads();
-    for (int a = threadIdx.x; a < kObsBlock; a += blockDim.x)
-        rinv[a] = a < bw ? 1.0f / Ub[a * kObsBlock + a] : 0.0f;
+    for (int a = threadIdx.x; a < kObsBlock; a += blockDim.x) {
+        const float ri = a < bw ? 1.0f / Ub[a * kObsBlock + a] : 0.0f;
+        rinv[a] = ri;
+        dsq[a] = ri * ri;
+    }
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ns = bw >> 5;
+    const int nq = bw >> 2;
+    const bool mine = 4 * lane < bw;  // this lane holds columns of the block
     for (int64_t r = (int64_t)blockIdx.x * kSweepWarps + warp; r < rows; r += (int64_t)gridDim.x * kSweepWarps) {
-        const int64_t base = r * K + i1;
-        float w0[4], w[4], p[4];
-        uint32_t keep[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const int64_t col = i1 + 32 * s + lane;
-            w0[s] = (s < ns && !dead[col]) ? __bfloat162float(W[base + 32 * s + lane]) : 0.0f;
-            p[s] = s < ns ? P[base + 32 * s + lane] : 0.0f;
-            w[s] = w0[s];
-            keep[s] = 0u;
+        const int64_t base = r * K + i1 + 4 * lane;
+        float w0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (mine) {
+            const uint2 wb = *reinterpret_cast<const uint2 *>(W + base);
+            const uchar4 dd = *reinterpret_cast<const uchar4 *>(dead + i1 + 4 * lane);
+            w0[0] = dd.x ? 0.0f : __uint_as_float(wb.x << 16);
+            w0[1] = dd.y ? 0.0f : __uint_as_float(wb.x & 0xFFFF0000u);
+            w0[2] = dd.z ? 0.0f : __uint_as_float(wb.y << 16);
+            w0[3] = dd.w ? 0.0f : __uint_as_float(wb.y & 0xFFFF0000u);
+            const float4 pv = *reinterpret_cast<const float4 *>(P + base);
+            p[0] = pv.x, p[1] = pv.y, p[2] = pv.z, p[3] = pv.w;
         }
+        float w[4] = {w0[0], w0[1], w0[2], w0[3]};
         // w += p U_bb  (row a of Ub holds zeros left of its diagonal)
+#pragma unroll 2
+        for (int qa = 0; qa < nq; ++qa) {
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            if (s >= ns)
-                break;
-#pragma unroll 4
-            for (int l = 0; l < 32; ++l) {
-                const float pa = __shfl_sync(0xffffffffu, p[s], l);
-                const float *urow = Ub + (32 * s + l) * kObsBlock;
-#pragma unroll
-                for (int s2 = s; s2 < 4; ++s2)
-                    w[s2] = fmaf(pa, urow[32 * s2 + lane], w[s2]);
+            for (int ta = 0; ta < 4; ++ta) {
+                const float pa = __shfl_sync(0xffffffffu, p[ta], qa);
+                const float4 u = *reinterpret_cast<const float4 *>(Ub + (4 * qa + ta) * kObsBlock + 4 * lane);
+                w[0] = fmaf(pa, u.x, w[0]);
+                w[1] = fmaf(pa, u.y, w[1]);
+                w[2] = fmaf(pa, u.z, w[2]);
+                w[3] = fmaf(pa, u.w, w[3]);
             }
         }
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            if (s >= ns)
-                break;
+        uint32_t kb = 0;  // this lane's keep bits (bit t = column 4 lane + t)
+        uint32_t kq = 0;  // keep bits of the current quad, the same in every lane
 #pragma unroll 1
-            for (int l = 0; l < 32; ++l) {
-                const int i = 32 * s + l;
-                if ((l & (M - 1)) == 0) {
-                    const float d = Ub[(32 * s + lane) * kObsBlock + 32 * s + lane];
-                    const float sc = w[s] * w[s] / (d * d);
-                    const int grp = lane & ~(M - 1);
-                    int rank = 0;
+        for (int q = 0; q < nq; ++q) {
 #pragma unroll
-                    for (int t = 0; t < M; ++t) {
-                        const float o = __shfl_sync(0xffffffffu, sc, grp + t);
-                        rank += (o > sc) || (o == sc && grp + t < lane);
+            for (int t = 0; t < 4; ++t) {
+                const int j = 4 * q + t;
+                if constexpr (M <= 4) {
+                    // the group is this quad's lane: every lane ranks its own
+                    // values, lane q's ranking is the one that counts
+                    if (t % M == 0) {
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int u = 0; u < M; ++u) {
+                            const float su = w[t + u] * w[t + u] * dsq[(4 * lane + t + u) & (kObsBlock - 1)];
+                            int rk = 0;
+#pragma unroll
+                            for (int u2 = 0; u2 < M; ++u2) {
+                                const float so = w[t + u2] * w[t + u2] * dsq[(4 * lane + t + u2) & (kObsBlock - 1)];
+                                rk += u2 != u && ((so > su) || (so == su && u2 < u));
+                            }
+                            bits |= rk < N ? 1u << (t + u) : 0u;
+                        }
+                        if (lane == q)
+                            kb |= bits;
+                        kq = __shfl_sync(0xffffffffu, kb, q);
                     }
-                    keep[s] |= __ballot_sync(0xffffffffu, grp == l && rank < N);
-                }
-                if (!((keep[s] >> l) & 1u)) {
-                    const float err = __shfl_sync(0xffffffffu, w[s], l) * rinv[i];
-                    const float *urow = Ub + i * kObsBlock;
+                } else {
+                    constexpr int G = M / 4;  // lanes per group
+                    if (t == 0) {
+                        if ((q & (G - 1)) == 0) {
+                            float sc[4];
 #pragma unroll
-                    for (int s2 = s; s2 < 4; ++s2)
-                        w[s2] = fmaf(-err, urow[32 * s2 + lane], w[s2]);
-                    if (lane == l)
-                        w[s] = 0.0f;
+                            for (int u = 0; u < 4; ++u)
+                                sc[u] = w[u] * w[u] * dsq[(4 * lane + u) & (kObsBlock - 1)];
+                            int rk[4] = {0, 0, 0, 0};
+#pragma unroll
+                            for (int m = 0; m < G; ++m)
+#pragma unroll
+                                for (int u2 = 0; u2 < 4; ++u2) {
+                                    const float o = __shfl_sync(0xffffffffu, sc[u2], q + m);
+                                    const int ocol = 4 * (q + m) + u2;
+#pragma unroll
+                                    for (int u = 0; u < 4; ++u)
+                                        rk[u] += (o > sc[u]) || (o == sc[u] && ocol < 4 * lane + u);
+                                }
+                            if ((lane & ~(G - 1)) == q)
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    kb |= rk[u] < N ? 1u << u : 0u;
+                        }
+                        kq = __shfl_sync(0xffffffffu, kb, q);
+                    }
+                }
+                if (!((kq >> t) & 1u)) {
+                    const float err = __shfl_sync(0xffffffffu, w[t], q) * rinv[j];
+                    const float4 u = *reinterpret_cast<const float4 *>(Ub + j * kObsBlock + 4 * lane);
+                    w[0] = fmaf(-err, u.x, w[0]);
+                    w[1] = fmaf(-err, u.y, w[1]);
+                    w[2] = fmaf(-err, u.z, w[2]);
+                    w[3] = fmaf(-err, u.w, w[3]);
+                    if (lane == q)
+                        w[t] = 0.0f;
                 }
             }
         }
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            if (s >= ns)
-                break;
-            Wout[base + 32 * s + lane] = __float2bfloat16_rn(w[s]);
+        if (mine) {
+            const uint32_t b01 = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[0])) |
+                                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[1])) << 16);
+            const uint32_t b23 = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[2])) |
+                                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[3])) << 16);
+            *reinterpret_cast<uint2 *>(Wout + base) = make_uint2(b01, b23);
             if (Wout_f32)
-                Wout_f32[base + 32 * s + lane] = w[s];
-            D[r * ldD + 32 * s + lane] = w0[s] - w[s];
-            if (masks && lane == 0)
-                masks[r * (K / 32) + i1 / 32 + s] = keep[s];
+                *reinterpret_cast<float4 *>(Wout_f32 + base) = make_float4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<float4 *>(D + r * ldD + 4 * lane) =
+                make_float4(w0[0] - w[0], w0[1] - w[1], w0[2] - w[2], w0[3] - w[3]);
+        }
+        if (masks) {
+            // word g (block columns 32 g .. 32 g + 31): bit 4 i + t from lane 8 g + i, bit t
+            const uint32_t k0 = __ballot_sync(0xffffffffu, kb & 1u), k1 = __ballot_sync(0xffffffffu, kb & 2u);
+            const uint32_t k2 = __ballot_sync(0xffffffffu, kb & 4u), k3 = __ballot_sync(0xffffffffu, kb & 8u);
+            if (lane < (bw >> 5)) {
+                const int sh = 8 * lane;
+                masks[r * (K / 32) + i1 / 32 + lane] = spread8(k0 >> sh) | (spread8(k1 >> sh) << 1) |
+                                                       (spread8(k2 >> sh) << 2) | (spread8(k3 >> sh) << 3);
+            }
         }
     }
 }
 
-constexpr size_t kSweepSmem = (size_t)kObsBlock * kObsBlock * 4 + kObsBlock * 4;
+constexpr size_t kSweepSmem = (size_t)kObsBlock * kObsBlock * 4 + 2 * kObsBlock * 4;
 
 struct SweepArgs {
     const __nv_bfloat16 *W;
