@@ -199,3 +199,15 @@ def test_obs_argument_validation_before_any_cuda_call(nm):
     assert hess(p16 + 2, 8, 64, p16, 0, None) == nm.NM_ERR_ALIGN
     assert hess(None, 0, 64, p16, 1, None) == nm.NM_OK  # nothing to add
     assert hess(None, 8, 0, None, 0, None) == nm.NM_OK
+
+
+def test_atomic_splitk_argument_validation(nm):
+    L = nm.lib()
+    buf = (ctypes.c_uint8 * 4096)()
+    p16 = (ctypes.addressof(buf) + 15) & ~15
+    f = L.nm_spmv_f32out_atomic
+    assert f(p16, p16, p16, p16, 4, 48, 1, None) == nm.NM_ERR_SHAPE
+    assert f(p16, p16, p16, p16, 4, 64, 9, None) == nm.NM_ERR_UNSUPPORTED
+    assert f(p16, p16, p16, p16 + 4, 4, 64, 1, None) == nm.NM_ERR_ALIGN
+    assert f(None, p16, p16, p16, 4, 64, 1, None) == nm.NM_ERR_INVALID_ARG
+    assert f(None, None, None, None, 0, 64, 1, None) == nm.NM_OK
