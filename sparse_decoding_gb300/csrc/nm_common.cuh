@@ -271,6 +271,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// Atomic add with acquire-release semantics at GPU scope: the caller's
+// earlier writes (and those ordered before them, e.g. by __syncwarp) become
+// visible to a thread that later reads the counter with acquire semantics.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ float ldcg_f32(const float *p)
 {
     float v;

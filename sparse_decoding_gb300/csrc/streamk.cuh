@@ -175,15 +175,16 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
 #pragma unroll
     for (int b = 0; b < B; ++b)
         mine[b * 32] = tot[b];
-    __threadfence();
+    // The warp's stores are ordered before lane 0's release; the CTA that
+    // counts last acquires every earlier part through the same counter.
     __syncwarp();
     uint32_t old = 0;
     if (lane == 0)
-        old = atomicAdd(&p.scratch.counters[first], 1u);
+        old = atom_add_acq_rel_gpu(&p.scratch.counters[first], 1u);
     old = __shfl_sync(0xFFFFFFFFu, old, 0);
     if (old != (uint32_t)(last - first))
         return;
-    __threadfence();
+    __syncwarp();
     float sum[B];
 #pragma unroll
     for (int b = 0; b < B; ++b)
