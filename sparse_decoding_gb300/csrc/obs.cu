@@ -618,12 +618,8 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     const int64_t nb = (K + kFacB - 1) / kFacB;
     if (!chol_inv(G, A, L, X, K, 0, nb, false, not_pd, st))
         return NM_ERR_CUDA;
-    int host_flag = 0;
-    if (cudaMemcpyAsync(&host_flag, not_pd, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return NM_ERR_CUDA;
-    if (host_flag)
-        return NM_ERR_NOT_PD;
+    // A pivot that is not positive was replaced by 1, so the rest runs on
+    // finite values; the flag is read once everything is queued.
     obs_reverse_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(L, K * K, R);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
@@ -660,7 +656,12 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
         if (s2 < K && !update(s2, K, s1, s2 - s1, Dbuf))
             return NM_ERR_CUDA;
     }
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    int host_flag = 0;
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(&host_flag, not_pd, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NM_ERR_CUDA;
+    return host_flag ? NM_ERR_NOT_PD : NM_OK;
 }
 
 }  // namespace
