@@ -712,7 +712,7 @@ def run_ours(args):
         "obs_pruning": pruning,
         "e2e": {"value": round(job_us_per_token(e2e_ms, world), 3), "unit": UNIT,
                 "h2d_bytes_per_step": x_all.numel() * 2, "d2h_bytes_per_step": y_all.numel() * 2,
-                "path": "pinned host x -> device, nm_stack_plan_run through the C ABI (no graph), y -> pinned host"},
+                "path": "pinned host x -> device, nm_stack_plan_run through the C ABI (the plan launches the CUDA graph of its chain captured at creation), y -> pinned host"},
         "gpu_launches": 4 * layers * args.steps,
         "clocks": sampler.summary(),
         "device_status": nm.status_str(status),

@@ -226,7 +226,11 @@ nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const v
  * nm_spmv_stack / dense_gemv_stack: op i+1 reads its x only after every part
  * of op i's y has been stored. Two ways to run it:
  *   default: one kernel per op, chained with programmatic dependent launch
- *     (as nm_spmv_stack; the fastest on GB300 for decode-sized ops);
+ *     (as nm_spmv_stack; the fastest on GB300 for decode-sized ops). The
+ *     chain is captured once into a CUDA graph when the plan is created, and
+ *     each run launches that graph (one host call instead of one per op);
+ *     a run on a stream that is itself being captured launches the kernels
+ *     one by one instead, so the caller's graph records them;
  *   NM_STACK_PERSISTENT: one persistent cooperative kernel walks all ops; a
  *     grid-wide barrier stands in for each kernel boundary, and each warp
  *     starts streaming the next op's weights before it arrives there. Used
@@ -237,7 +241,8 @@ nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const v
  *   the call; each op as for nm_spmv, or dense_gemv with NM_STACK_DENSE, with
  *   `batch` rows of x) and prepares the plan; with NM_STACK_PERSISTENT it
  *   encodes every op's descriptors into device memory that the plan owns
- *   (cudaMalloc; synchronous). The plan holds the ops' device pointers: the
+ *   (cudaMalloc; synchronous); by default it captures the chained launches
+ *   on a private stream (nothing runs). The plan holds the ops' device pointers: the
  *   buffers must stay allocated, and each run reads and writes whatever they
  *   hold then. Make this call outside CUDA graph capture, on the device the
  *   plan will run on. *plan is set on NM_OK only. Errors: those of the per-op

@@ -208,7 +208,35 @@ struct nm_stack_plan {
     StackOp *ops_dev = nullptr;
     uint32_t *gbar = nullptr;
     std::vector<nm_linear> ops; // host copy for the chained path
+    cudaGraphExec_t exec = nullptr; // the chained launches, captured once
 };
+
+// Capture the plan's chained launches (PDL edges included) into a graph on a
+// private stream. On any failure the plan keeps launching directly.
+static void capture_chain(nm_stack_plan *pl)
+{
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    cudaGraph_t g = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        nm_status s = pl->dense ? dense_gemv_stack(pl->ops.data(), pl->n_ops, pl->batch, cs)
+                                : nm_spmv_stack(pl->ops.data(), pl->n_ops, pl->batch, cs);
+        if (cudaStreamEndCapture(cs, &g) != cudaSuccess || s != NM_OK) {
+            if (g)
+                cudaGraphDestroy(g);
+            g = nullptr;
+        }
+    }
+    if (g && cudaGraphInstantiate(&pl->exec, g, 0) != cudaSuccess)
+        pl->exec = nullptr;
+    if (g)
+        cudaGraphDestroy(g);
+    cudaStreamDestroy(cs);
+    cudaGetLastError(); // a failed capture leaves no error behind
+}
 
 extern "C" {
 
@@ -400,6 +428,8 @@ nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsig
             return s;
         }
     }
+    if (!fits && n_ops > 0)
+        capture_chain(pl);
     *plan = pl;
     return NM_OK;
 }
@@ -413,9 +443,15 @@ nm_status nm_stack_plan_run(const nm_stack_plan *plan, void *stream)
         return NM_ERR_CUDA;
     if (dev != plan->dev)
         return NM_ERR_INVALID_ARG;
-    if (!plan->persistent)
+    if (!plan->persistent) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (plan->exec && cudaStreamIsCapturing((cudaStream_t)stream, &cap) == cudaSuccess &&
+            cap == cudaStreamCaptureStatusNone)
+            return cudaGraphLaunch(plan->exec, (cudaStream_t)stream) == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+        cudaGetLastError();
         return plan->dense ? dense_gemv_stack(plan->ops.data(), plan->n_ops, plan->batch, stream)
                            : nm_spmv_stack(plan->ops.data(), plan->n_ops, plan->batch, stream);
+    }
     LaunchCtx ctx;
     nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
     if (s != NM_OK)
@@ -432,6 +468,15 @@ nm_status nm_stack_plan_destroy(nm_stack_plan *plan)
     if (!plan)
         return NM_OK;
     nm_status s = NM_OK;
+    if (plan->exec) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(plan->dev);
+        if (cudaDeviceSynchronize() != cudaSuccess || cudaGraphExecDestroy(plan->exec) != cudaSuccess)
+            s = NM_ERR_CUDA;
+        if (cur >= 0)
+            cudaSetDevice(cur);
+    }
     if (plan->dmem) {
         int cur = -1;
         cudaGetDevice(&cur);
