@@ -43,7 +43,6 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
-#include <vector>
 
 #include "nmspmv.h"
 
@@ -54,7 +53,7 @@ constexpr int kObsBlock = 128;   // columns per sweep block
 constexpr int kSuper = 1024;     // columns per lazy-update superblock (a multiple of kObsBlock)
 constexpr int kSweepWarps = 16;  // rows in flight per CTA
 constexpr int kMaxDevices = 64;
-const float kOne = 1.0f, kMinusOne = -1.0f;
+const float kOne = 1.0f;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
