@@ -615,3 +615,26 @@ def test_swiglu_op_feeds_down_in_a_stack(nm, persistent):
 
 def test_no_bounded_wait_ran_out(nm):
     assert nm.device_status() == nm.NM_OK
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_plan_reads_current_inputs_each_run(nm, batch):
+    """The chained plan replays a graph captured at creation: each run must read
+    x as it is then (no values are frozen into the graph), on any stream."""
+    ops_s, _, refs = _stack_inputs(nm, batch, layers=1)
+    plan = nm.StackPlan(ops_s, batch)
+    for trial in range(3):
+        for i, op in enumerate(ops_s):
+            op["x"].copy_(synth.activations(batch, op["K"], seed=700 + 10 * trial + i).cuda())
+            op["y"].fill_(float("nan"))
+        s = torch.cuda.Stream() if trial == 2 else torch.cuda.current_stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            plan.run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for i, (op, (_, _, _, W)) in enumerate(zip(ops_s, refs)):
+            y64, S = oracle.spmv_f64(to_bits(W.cpu()), to_bits(op["x"].cpu()))
+            check_bf16(to_bits(op["y"]), y64, S, f"plan run {trial} op {i} b{batch}")
+    plan.close()
+    assert nm.device_status() == nm.NM_OK
