@@ -331,6 +331,15 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor TFLOP/s: the burst figure of MEASURED_PEAKS.json, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def recorded_traffic():
     """dram bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
     try:
@@ -498,12 +507,20 @@ def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True, linears=s
                      "fp32_tflops_effective": round(f / (best[1] * 1e-3) / 1e12, 2)}
         del W, X, H, Wp, masks, values
     total_ms = sum(v["hessian_ms"] + v["prune_ms"] + v["pack_ms"] for v in per.values())
+    bf16, bf16_kind = measured_bf16_peak()
+    emu_peak = bf16 / 9.0  # cuBLAS runs 9 bf16 products per emulated fp32 product
+    achieved = total_flops / (sum(v["prune_ms"] for v in per.values()) * 1e-3) / 1e12
     out = {"workload": f"{'one ' + model + ' decoder layer' if len(per) == 4 else model + ' ' + ', '.join(per)} "
                        f"pruned {N}:{M} by the OBS rule, each linear against the "
                        f"Hessian of {tokens} synthetic calibration tokens, then packed",
            "ms_per_layer": round(total_ms, 2), "hessian_ms": round(hess_ms, 3),
            "fp32_tflops_effective": round(total_flops / (sum(v["prune_ms"] for v in per.values()) * 1e-3) / 1e12, 2),
            "algorithmic_flops": f"{total_flops:.4g} (2 K^3 / 3 + rows K^2 / 2 per linear)",
+           "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(emu_peak, 1),
+                        "unit": "TFLOP/s", "frac": round(achieved / emu_peak, 4),
+                        "peak_basis": f"{bf16_kind} bf16 {bf16} TFLOP/s / 9 (fp32 emulated on the bf16 tensor "
+                                      "cores, 9 bf16 products per fp32 product); achieved = algorithmic fp32 flops "
+                                      "/ event-timed prune time"},
            "per_linear": per}
     if cpu:
         sys.path.insert(0, ROOT)
@@ -547,11 +564,14 @@ def splitk_compare(nm, stack, pattern, world, steps, warmup):
                 t, _ = time_graph(g, steps, warmup, world)
                 res["atomic" if atomic else "deterministic"] = t * 1e3 / len(idx)
                 del g
-            by = sparse_bytes(rows, K, b)
+            by = sparse_bytes(rows, K, b) + 2 * rows * b  # fp32 y: 2 more bytes per output than bf16
+            peak = measured_peak()[0]
             out[f"{name} {rows}x{K} batch {b}"] = {
                 "deterministic_us": round(res["deterministic"], 3), "atomic_us": round(res["atomic"], 3),
                 "deterministic_GB_s": round(by / (res["deterministic"] * 1e-6) / 1e9, 1),
-                "atomic_GB_s": round(by / (res["atomic"] * 1e-6) / 1e9, 1)}
+                "atomic_GB_s": round(by / (res["atomic"] * 1e-6) / 1e9, 1),
+                "frac_of_measured_peak": {"deterministic": round(by / (res["deterministic"] * 1e-6) / 1e9 / peak, 4),
+                                          "atomic": round(by / (res["atomic"] * 1e-6) / 1e9 / peak, 4)}}
             del xs, ys
     return out
 
