@@ -111,16 +111,21 @@ constexpr int kFacThreads = 512;  // 4 row groups x 128 columns
 // below the diagonal. A block narrower than 128 is padded with the identity.
 //
 // Phase 1, the factorisation: thread t = 128 g + r holds row r, columns
-// 32 g .. 32 g + 31, of the working block in registers. Step j publishes
-// column j (one shared store per thread of group j / 32, double buffered so
-// that one barrier per step suffices), then applies a_rc -= a_rj a_cj / a_jj
-// to columns c > j. Only entries on or below the diagonal of column j are
+// 32 g .. 32 g + 31, of the working block in registers. Each step takes two
+// pivots j, j + 1: the two columns are published as they stand (one shared
+// store each per thread of group j / 32, double buffered so that one barrier
+// per step suffices); every thread applies pivot j to the entries of column
+// j + 1 it reads, then the rank-2 update
+// a_rc -= a_rj a_cj / a_jj + a'_r(j+1) a'_c(j+1) / a'_(j+1)(j+1) to columns
+// c > j + 1. Only entries on or below the diagonal of columns j, j + 1 are
 // read, so rows already passed may take meaningless updates; warps whose rows
-// are all passed skip the step. Column j of L (a_rj / sqrt(a_jj)) and
+// are all passed, or lie above their columns, skip the step. Column j of L (a_rj / sqrt(a_jj)) and
 // 1 / L_jj go to shared memory. A pivot that is not positive sets *not_pd and
 // is replaced by 1.
-// Phase 2, the inverse (forward substitution L X = I, right-looking): lanes
-// 4c .. 4c + 3 of the CTA hold column c of X, lane q rows 4 m + q. Step k
+// Phase 2, the inverse (forward substitution L X = I, right-looking): four
+// lanes of one warp hold a column c of X, lane q its rows 4 m + q; each warp
+// takes one column group from the left half and one from the right half, so
+// the warps' shares are even. Step k
 // finalises X_kc = x_kc / L_kk (shuffled from its owner lane) and applies
 // x_ic -= L_ik X_kc to rows i > k. No barrier is needed: a column lives in one
 // warp. A warp skips the steps k left of its columns, where X_kc = 0.
@@ -132,6 +137,7 @@ __global__ void __launch_bounds__(kFacThreads, 1)
 {
     extern __shared__ float Ls[];  // [128][129]: L_kk, row-major, padded
     __shared__ __align__(16) float colA[2][kFacB];
+    __shared__ __align__(16) float colB[2][kFacB];
     __shared__ float rdiag[kFacB];
     constexpr int P = kFacB + 1;
     {
@@ -153,25 +159,43 @@ __global__ void __launch_bounds__(kFacThreads, 1)
 #pragma unroll 1
         for (int gj = 0; gj < 4; ++gj) {
 #pragma unroll
-            for (int mj = 0; mj < 32; ++mj) {
-                const int j = 32 * gj + mj, buf = mj & 1;
-                if (g == gj)
+            for (int mp = 0; mp < 16; ++mp) {
+                // pivots j and j + 1 together: both columns are published as
+                // they stand before step j, and every thread applies step j to
+                // the entries of column j + 1 that it needs
+                const int mj = 2 * mp, j = 32 * gj + mj, buf = mp & 1;
+                if (g == gj) {
                     colA[buf][r] = a[mj];
+                    colB[buf][r] = a[mj + 1];
+                }
                 __syncthreads();
                 const float d0 = colA[buf][j];
-                bad |= !(d0 > 0.0f);
-                const float rs = rsqrtf(d0 > 0.0f ? d0 : 1.0f), rd = rs * rs;
+                const float rs0 = rsqrtf(d0 > 0.0f ? d0 : 1.0f), rd0 = rs0 * rs0;
+                const float t = colA[buf][j + 1] * rd0;  // column j+1 -= column j * t
+                const float d1 = colB[buf][j + 1] - colA[buf][j + 1] * t;
+                bad |= !(d0 > 0.0f) || !(d1 > 0.0f);
+                const float rs1 = rsqrtf(d1 > 0.0f ? d1 : 1.0f), rd1 = rs1 * rs1;
                 if (g == gj) {
-                    Ls[r * P + j] = r >= j ? a[mj] * rs : 0.0f;
+                    const float b1 = a[mj + 1] - a[mj] * t;
+                    Ls[r * P + j] = r >= j ? a[mj] * rs0 : 0.0f;
+                    Ls[r * P + j + 1] = r >= j + 1 ? b1 * rs1 : 0.0f;
                     if (r == j)
-                        rdiag[j] = rs;
+                        rdiag[j] = rs0;
+                    if (r == j + 1)
+                        rdiag[j + 1] = rs1;
                 }
-                if (g >= gj && rw0 + 31 > j) {
-                    const float ci = colA[buf][r] * rd;
+                // warps whose rows lie above their columns hold only the upper
+                // triangle, which nothing reads
+                if (g >= gj && rw0 + 31 > j && rw0 >= 32 * g) {
+                    const float ca = colA[buf][r], cb = colB[buf][r] - ca * t;
+                    const float ci0 = ca * rd0, ci1 = cb * rd1;
 #pragma unroll
                     for (int m = 0; m < 32; ++m)
-                        if (g > gj || m > mj)
-                            a[m] = fmaf(-ci, colA[buf][32 * g + m], a[m]);
+                        if (g > gj || m > mj + 1) {
+                            const float xa = colA[buf][32 * g + m];
+                            const float xb = colB[buf][32 * g + m] - xa * t;
+                            a[m] = fmaf(-ci1, xb, fmaf(-ci0, xa, a[m]));
+                        }
                 }
             }
         }
@@ -180,18 +204,20 @@ __global__ void __launch_bounds__(kFacThreads, 1)
     }
     __syncthreads();
     {
-        const int c = threadIdx.x >> 2, q = threadIdx.x & 3, lane = threadIdx.x & 31;
-        const int cmin = (threadIdx.x & ~31) >> 2;  // this warp's columns: cmin .. cmin + 7
+        // warp w holds columns 4w .. 4w+3 (lanes 0-15) and 124-4w .. 127-4w
+        // (lanes 16-31): a long and a short forward substitution per warp
+        const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5, q = lane & 3;
+        const int c = lane < 16 ? 4 * wq + (lane >> 2) : 124 - 4 * wq + ((lane - 16) >> 2);
+        const int cmin = 4 * wq;  // this warp's leftmost column
         float x[32];
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             x[m] = (4 * m + q == c) ? 1.0f : 0.0f;
-        // k = 4 kk + kq: the register index kk is unrolled, kq is a loop
 #pragma unroll
         for (int kk = 0; kk < 32; ++kk) {
             if (4 * kk + 3 < cmin)
                 continue;
-#pragma unroll 1
+#pragma unroll
             for (int kq = 0; kq < 4; ++kq) {
                 const int k = 4 * kk + kq;
                 const float xk = __shfl_sync(0xffffffffu, x[kk], (lane & ~3) | kq) * rdiag[k];
