@@ -213,11 +213,13 @@ __global__ void __launch_bounds__(kFacThreads, 1)
 #pragma unroll
         for (int m = 0; m < 32; ++m)
             x[m] = (4 * m + q == c) ? 1.0f : 0.0f;
+        // k = 4 kk + kq: the register index kk is unrolled, kq stays a loop
+        // (the code stays small; it runs between cuBLAS kernels, cold)
 #pragma unroll
         for (int kk = 0; kk < 32; ++kk) {
             if (4 * kk + 3 < cmin)
                 continue;
-#pragma unroll
+#pragma unroll 1
             for (int kq = 0; kq < 4; ++kq) {
                 const int k = 4 * kk + kq;
                 const float xk = __shfl_sync(0xffffffffu, x[kk], (lane & ~3) | kq) * rdiag[k];
