@@ -426,8 +426,13 @@ static nm_status launch_tma(const uint32_t *masks, const void *values, const voi
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows, KC = K / kSpCols;
     if constexpr (B <= 2) {
         // Few, long row blocks (at most one per SM, 64+ units each): one CTA
-        // of 16 warps per row block halves each warp's share of it.
-        if (nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
+        // of 16 warps per row block halves each warp's share of it -- unless,
+        // at batch 1, CTA pairs can split the row blocks' K instead: that
+        // halves the share as well and also puts the SMs to work that whole
+        // row blocks would leave idle (down of the 8B stack: 128 row blocks,
+        // 152 SMs; -5% per layer).
+        const bool pairs = B == 1 && pair_split_ok<SparseCfg<1>::W, SparseCfg<1>::MINB>(nrb, KC, ctx.num_sms);
+        if (!pairs && nrb <= ctx.num_sms && KC >= 64 && choose_split(nrb, KC, 16, 1, ctx.num_sms).whole)
             return launch_streamk<SparseUnit, B, 16, 2, 1, OUT>(maps, y, rows, KC, ctx);
     }
     return launch_streamk<SparseUnit, B, SparseCfg<B>::W, SparseCfg<B>::NBUF, SparseCfg<B>::MINB, OUT>(

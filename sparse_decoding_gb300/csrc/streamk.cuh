@@ -952,6 +952,15 @@ inline Split choose_split(int64_t nrb, int64_t KC, int W, int minb, int num_sms)
     return choose_split_slots(nrb, KC, W, (int64_t)num_sms * minb);
 }
 
+// Batch 1: whether CTA pairs (clusters of 2) split each row block's K in
+// halves -- few row blocks (at most half the CTA slots) whose halves fit the
+// shared unit queue.
+template <int W, int MINB> inline bool pair_split_ok(int64_t nrb, int64_t KC, int num_sms)
+{
+    return MINB == 2 && 2 * nrb <= (int64_t)num_sms * MINB && KC % 2 == 0 && KC / 2 >= 2 &&
+           KC / 2 <= queue_cap<W>() && KC < 32768;
+}
+
 // Launch the stream-K kernel for a problem of `rows` rows and KC units per row
 // block. MINB CTAs of W warps share an SM, so that at a kernel boundary the
 // next kernel's CTAs can take the place of this kernel's first finishers and
@@ -988,8 +997,7 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     // Few row blocks (at most half the CTA slots) at batch 1: split each row
     // block's K over a CTA pair, so that each warp's share is half as long.
     const int64_t slots = (int64_t)ctx.num_sms * MINB;
-    p.pair_k = (B == 1 && MINB == 2 && 2 * nrb <= slots && KC % 2 == 0 && KC / 2 >= 2 && KC / 2 <= queue_cap<W>() &&
-                KC < 32768) ? 1 : 0;
+    p.pair_k = (B == 1 && pair_split_ok<W, MINB>(nrb, KC, ctx.num_sms)) ? 1 : 0;
     int64_t grid = ctas;
     if (p.pair_k) {
         p.shared_queue = 1;
