@@ -122,20 +122,30 @@ constexpr int kFacThreads = 512;  // 4 row groups x 128 columns
 // are all passed, or lie above their columns, skip the step. Column j of L (a_rj / sqrt(a_jj)) and
 // 1 / L_jj go to shared memory. A pivot that is not positive sets *not_pd and
 // is replaced by 1.
-// Phase 2, the inverse (forward substitution L X = I, right-looking): four
-// lanes of one warp hold a column c of X, lane q its rows 4 m + q; each warp
-// takes one column group from the left half and one from the right half, so
-// the warps' shares are even. Step k
-// finalises X_kc = x_kc / L_kk (shuffled from its owner lane) and applies
-// x_ic -= L_ik X_kc to rows i > k. No barrier is needed: a column lives in one
-// warp. A warp skips the steps k left of its columns, where X_kc = 0.
-constexpr size_t kFacSmem = (size_t)kFacB * (kFacB + 1) * 4;
+// Phase 2, the inverse X = L^-1 in 32 x 32 blocks: four warps invert the
+// diagonal blocks (forward substitution, lane = column, rows in registers);
+// the blocks below follow in three waves, X_ij = -X_ii sum_k L_ik X_kj, as
+// 8-row x 32-column tile products in shared memory spread over the warps.
+constexpr size_t kFacSmem = (size_t)2 * kFacB * (kFacB + 1) * 4 + 3 * 32 * 33 * 4;
+
+// acc[r] += sum_k A[r][k] B[k][lane] for 8 rows of A and 32 columns of B
+// (lane = column); A, B in shared memory with row strides lda, ldb.
+__device__ __forceinline__ void tile_mm8(const float *A, int lda, const float *B, int ldb, float (&acc)[8], int lane)
+{
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+        const float b = B[k * ldb + lane];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            acc[r] = fmaf(A[r * lda + k], b, acc[r]);
+    }
+}
 
 __global__ void __launch_bounds__(kFacThreads, 1)
     fac_diag_kernel(const float *__restrict__ A, float *__restrict__ X, int64_t K, int64_t k0, int kb,
                     int *__restrict__ not_pd)
 {
-    extern __shared__ float Ls[];  // [128][129]: L_kk, row-major, padded
+    extern __shared__ float Ls[];  // [128][129]: L_kk, row-major, padded; then X and scratch
     __shared__ __align__(16) float colA[2][kFacB];
     __shared__ __align__(16) float colB[2][kFacB];
     __shared__ float rdiag[kFacB];
@@ -204,39 +214,61 @@ __global__ void __launch_bounds__(kFacThreads, 1)
     }
     __syncthreads();
     {
-        // warp w holds columns 4w .. 4w+3 (lanes 0-15) and 124-4w .. 127-4w
-        // (lanes 16-31): a long and a short forward substitution per warp
-        const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5, q = lane & 3;
-        const int c = lane < 16 ? 4 * wq + (lane >> 2) : 124 - 4 * wq + ((lane - 16) >> 2);
-        const int cmin = 4 * wq;  // this warp's leftmost column
-        float x[32];
+        // Phase 2 in 32 x 32 blocks: X_pp = L_pp^-1, then for i > j
+        // X_ij = -X_ii sum_{k=j}^{i-1} L_ik X_kj, in waves of i - j = 1, 2, 3.
+        float *Xs = Ls + kFacB * P;  // X, row-major, padded
+        float *Tb = Xs + kFacB * P;  // three 32 x 33 scratch tiles
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        if (w < 4) {
+            // warp p inverts L_pp; lane c holds column c (rows in registers)
+            const int o = 32 * w;
+            float x[32];
 #pragma unroll
-        for (int m = 0; m < 32; ++m)
-            x[m] = (4 * m + q == c) ? 1.0f : 0.0f;
-        // k = 4 kk + kq: the register index kk is unrolled, kq stays a loop
-        // (the code stays small; it runs between cuBLAS kernels, cold)
+            for (int i = 0; i < 32; ++i)
+                x[i] = (i == lane) ? 1.0f : 0.0f;
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk) {
-            if (4 * kk + 3 < cmin)
-                continue;
-#pragma unroll 1
-            for (int kq = 0; kq < 4; ++kq) {
-                const int k = 4 * kk + kq;
-                const float xk = __shfl_sync(0xffffffffu, x[kk], (lane & ~3) | kq) * rdiag[k];
-                if (q == kq)
-                    x[kk] = xk;
-                else if (q > kq)
-                    x[kk] = fmaf(-Ls[(4 * kk + q) * P + k], xk, x[kk]);
+            for (int k = 0; k < 32; ++k) {
+                const float xk = x[k] * rdiag[o + k];
+                x[k] = xk;
 #pragma unroll
-                for (int m = kk + 1; m < 32; ++m)
-                    x[m] = fmaf(-Ls[(4 * m + q) * P + k], xk, x[m]);
+                for (int i = k + 1; i < 32; ++i)
+                    x[i] = fmaf(-Ls[(o + i) * P + o + k], xk, x[i]);
             }
-        }
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
-            const int i = 4 * m + q;
-            if (i < kb && c < kb)
-                X[(k0 + i) * K + k0 + c] = x[m];
+            for (int i = 0; i < 32; ++i)
+                Xs[(o + i) * P + o + lane] = x[i];
+        }
+        __syncthreads();
+        // warp w works on rows 8 (w & 3) .. + 7 of tile slot w >> 2
+        const int slot = w >> 2, r0 = 8 * (w & 3);
+        auto T = [&](int s) { return Tb + s * 32 * 33; };
+#pragma unroll 1
+        for (int d = 1; d <= 3; ++d) {
+            const int j = slot, i = slot + d;  // block (i, j) of this wave
+            const bool active = i < 4;
+            if (active) {
+                float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (int k = j; k < i; ++k)
+                    tile_mm8(Ls + (32 * i + r0) * P + 32 * k, P, Xs + (32 * k) * P + 32 * j, P, acc, lane);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    T(slot)[(r0 + r) * 33 + lane] = acc[r];
+            }
+            __syncthreads();
+            if (active) {
+                float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                tile_mm8(Xs + (32 * i + r0) * P + 32 * i, P, T(slot), 33, acc, lane);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    Xs[(32 * i + r0 + r) * P + 32 * j + lane] = -acc[r];
+            }
+            __syncthreads();
+        }
+        // the blocks on and below the diagonal (X's upper part is zero on entry)
+        for (int q = threadIdx.x; q < kFacB * kFacB; q += blockDim.x) {
+            const int i = q / kFacB, c = q % kFacB;
+            if ((c >> 5) <= (i >> 5) && i < kb && c < kb)
+                X[(k0 + i) * K + k0 + c] = Xs[i * P + c];
         }
     }
 }
