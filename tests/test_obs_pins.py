@@ -140,3 +140,26 @@ def test_keep_words_bit_order():
     keep[1, 63] = True
     w = obs.keep_words(keep)
     assert w.tolist() == [[0x80000001, 0x2], [0, 0x80000000]]
+
+
+def test_random_cases_match_least_squares():
+    """Property check over random small layers: patterns with M in {2, 4, 8},
+    1 <= N <= M, damping 0.001-0.2, token counts below and above K, dead inputs."""
+    hyp = pytest.importorskip("hypothesis")
+    st = hyp.strategies
+
+    @hyp.settings(max_examples=25, deadline=None, derandomize=True)
+    @hyp.given(st.sampled_from([2, 4, 8]), st.integers(1, 8), st.integers(1, 3), st.integers(4, 40),
+               st.floats(0.001, 0.2), st.integers(0, 10_000), st.booleans())
+    def check(M, N, kgroups, T, percdamp, seed, with_dead):
+        N = min(N, M)
+        K = 8 * kgroups
+        dead = (1,) if with_dead else ()
+        W0, H0 = _case(3, K, T, seed=seed, dead=dead)
+        Wo, ko = obs.obs_prune_f64(W0, H0, N, M, percdamp)
+        Wl, kl = _lsq_prune(W0, H0, N, M, percdamp)
+        assert np.array_equal(ko, kl)
+        assert np.allclose(Wo, Wl, rtol=1e-8, atol=1e-11 * max(np.abs(W0).max(), 1e-30))
+        assert np.all(ko.reshape(3, -1, M).sum(axis=2) == N)
+
+    check()
