@@ -349,13 +349,14 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  *                 is set when column 32g + j is kept (the decode mask format).
  *   W_out_f32   : device, fp32 [rows][K] or NULL (written): the pruned weights
  *                 in fp32, before the rounding to bf16.
- * Arithmetic is fp32: the Cholesky factorisation of the reversed Hessian, its
- * triangular inverse and the column sweep run in this library's kernels, their
- * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K + 4096 rows bytes, taken from the stream-ordered allocator and
- * returned before the call ends. SYNCHRONOUS: returns after the
- * result is written (NM_ERR_NOT_PD when the damped Hessian cannot be
- * factorised; outputs are then unspecified). Calls on one device are
- * serialized by a lock. Pointers 16-byte aligned (NM_ERR_ALIGN).
+ * Arithmetic is fp32: the Cholesky factorisation of the reversed Hessian, the
+ * inverses it needs and the column sweep run in this library's kernels, their
+ * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K + 4096 rows
+ * bytes, taken from the stream-ordered allocator and returned before the call
+ * ends. SYNCHRONOUS: returns after the result is written (NM_ERR_NOT_PD when
+ * the damped Hessian cannot be factorised; outputs are then unspecified).
+ * Calls on one device are serialized by a lock. Pointers 16-byte aligned
+ * (NM_ERR_ALIGN).
  */
 nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t rows, int64_t K, int N, int M, float percdamp,
                        unsigned flags, void *W_out_bf16, uint32_t *keep_masks, float *W_out_f32, void *stream);
