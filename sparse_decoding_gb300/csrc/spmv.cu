@@ -108,40 +108,27 @@ __device__ __forceinline__ void walk_unit_b1(const uint32_t (&m)[4], const uint3
 constexpr uint32_t kIrregular = 0x80u;
 constexpr int kLutBytes = 4 * 256 * 4;
 
-// The four tables, computed at compile time into the library image. Copied
-// with 16-byte loads, so the object is 16-byte aligned.
-struct alignas(16) ByteTables {
-    uint32_t v[4 * 256];
-    constexpr ByteTables() : v()
-    {
-        for (int i = 0; i < 4 * 256; ++i) {
-            const int b = i >> 8, e = i & 255;
-            int bits = 0;
-            for (int j = 0; j < 8; ++j)
-                bits += (e >> j) & 1;
-            uint32_t ent = kIrregular;
-            if (bits == 4) {
-                ent = 0;
-                int k = 0;
-                for (int j = 0; j < 8; ++j)
-                    if ((e >> j) & 1) {
-                        ent |= (uint32_t)(8 * b + j) << (8 * k);
-                        ++k;
-                    }
-            }
-            v[i] = ent;
-        }
-    }
-};
-static_assert(alignof(ByteTables) == 16 && sizeof(ByteTables) == kLutBytes, "table layout");
-__device__ const ByteTables kByteTables{};
-
-// Copy the tables into the CTA's shared memory (16 bytes per thread-step;
-// `lut` is 16-byte aligned).
+// Each CTA computes the four tables into its shared memory (a few dozen
+// instructions per entry, no memory reads): a copy from global memory sat on
+// the critical path of a CTA's start whenever HBM was busy with the previous
+// kernel's traffic, and every CTA of the grid read the same 4 KB at once.
 __device__ __forceinline__ void init_byte_tables(uint32_t *lut, int tid, int nthreads)
 {
-    for (int i = tid; i < kLutBytes / 16; i += nthreads)
-        ((uint4 *)lut)[i] = ((const uint4 *)kByteTables.v)[i];
+    for (int i = tid; i < 4 * 256; i += nthreads) {
+        const uint32_t b = (uint32_t)i >> 8;
+        uint32_t e = (uint32_t)i & 255u;
+        uint32_t ent = kIrregular;
+        if (__popc(e) == 4) {
+            ent = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t j = (uint32_t)(__ffs(e) - 1); // position of the k-th set bit
+                e &= e - 1;
+                ent |= (8 * b + j) << (8 * k);
+            }
+        }
+        lut[i] = ent;
+    }
 }
 
 // Batch 1, byte-regular words: looked-up columns, x gathered by warp shuffle
