@@ -236,17 +236,33 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
     const int64_t n = cr.ce - cr.cs;
     const int first = (int)div64(((lo - cr.cs + 1) * (cr.nw)) - 1, n);
     const int last = (int)div64(((hi - cr.cs) * (cr.nw)) - 1, n);
+    // Every contributor after the first starts its range inside rb, so rb is
+    // its first row block (slot 0); the first contributor's slot is 1 when its
+    // range began in an earlier row block. (One division for the whole row
+    // block: a division per contributor made this loop cost microseconds.)
+    const int slot_first = (cr.cs + muldiv(n, first, cr.nw) < lo) ? 1 : 0;
     float tot[B];
 #pragma unroll
     for (int b = 0; b < B; ++b)
         tot[b] = 0.f;
-    for (int w = first; w <= last; ++w) {
-        const int64_t w_rb0 = div64(cr.cs + muldiv(n, w, cr.nw), KC);
-        const int ws = (rb == w_rb0) ? 0 : 1;
-        const float *q = part + ((w * 2 + ws) * B) * 32 + lane;
+    // Up to four contributors' loads in flight, added in warp order (a missing
+    // one adds +0, which leaves the sum unchanged: it never is -0).
+    for (int w0 = first; w0 <= last; w0 += 4) {
+        float v[4][B];
 #pragma unroll
-        for (int b = 0; b < B; ++b)
-            tot[b] += q[b * 32];
+        for (int j = 0; j < 4; ++j) {
+            const int w = w0 + j;
+            const int ws = w == first ? slot_first : 0;
+            const float *q = part + ((w * 2 + ws) * B) * 32 + lane;
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                v[j][b] = w <= last ? q[b * 32] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                tot[b] += v[j][b];
     }
     finish_across_ctas<B, OUT>(p, cr, rb, tot, lane);
 }

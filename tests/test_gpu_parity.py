@@ -516,6 +516,26 @@ def test_plan_repeats_and_graph_replay_bit_exact(nm, persistent):
     assert nm.device_status() == nm.NM_OK
 
 
+def test_plans_of_different_sizes_interleave(nm):
+    # a persistent plan with many ops, then one with a single op (less shared
+    # memory), then both run: creating the small plan must not break the large one
+    ops_s, _, refs = _stack_inputs(nm, 1)
+    big = nm.StackPlan(ops_s, 1, persistent=True)
+    small = nm.StackPlan(ops_s[:1], 1, persistent=True)
+    for op in ops_s:
+        op["y"].fill_(float("nan"))
+    big.run()
+    small.run()
+    big.run()
+    torch.cuda.synchronize()
+    for i, (op, (_, _, x, W)) in enumerate(zip(ops_s, refs)):
+        y64, S = oracle.spmv_f64(to_bits(W.cpu()), to_bits(x.cpu()))
+        check_bf16(to_bits(op["y"]), y64, S, f"large plan op {i}")
+    big.close()
+    small.close()
+    assert nm.device_status() == nm.NM_OK
+
+
 def test_plan_falls_back_to_chained_launches(nm):
     # K = 96 is off the TMA path: the plan runs the ops as nm_spmv_stack would
     ops_s, _, refs = _stack_inputs(nm, 2, layers=1)
