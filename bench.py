@@ -62,6 +62,9 @@ def parse_args():
                     help="run only the OBS pruning measurement and print its JSON object")
     ap.add_argument("--prune-linears", default="qkv,o,gate_up,down", help="linears to prune (comma list)")
     ap.add_argument("--prune-repeats", type=int, default=2, help="timed repeats per linear (after one untimed)")
+    ap.add_argument("--suite", action="store_true",
+                    help="run the larger model stacks instead (Qwen3-14B/32B at 4:8 and 8:16, batch 1; "
+                         "Llama-3.3-70B at 2:4 and 16:32, batch 1/2/4/8) and print their JSON object")
     return ap.parse_args()
 
 
@@ -184,9 +187,16 @@ class ClockSampler:
 # --- workload ---------------------------------------------------------------------------------
 
 class Stack:
-    """All linears of one decode token: weights packed per pattern, x/y per batch size."""
+    """All linears of one decode token: weights packed per pattern, x/y per batch size.
 
-    def __init__(self, nm, model: str, patterns, batches, layers: int, keep_dense: bool, seed: int = 0):
+    Each linear's W and column norms a are drawn on the GPU; every pattern is
+    selected and packed from the same W in one pass (nm_select_pack). The dense
+    references keep W itself (the dense model's weights). With swiglu, the
+    gate_up linears of the first pattern are also packed in the gate/up pair
+    layout of the SwiGLU epilogue."""
+
+    def __init__(self, nm, model: str, patterns, batches, layers: int, keep_dense: bool, seed: int = 0,
+                 swiglu: bool = True):
         shapes = synth.MODELS[model]
         self.model = model
         self.layers = layers or shapes["layers"]
@@ -200,14 +210,13 @@ class Stack:
                 W = synth.weights(rows, K, seed, synth.stream_id(CONFIG_ID, layer, mi, 0), device="cuda")
                 a = synth.col_norms(K, seed, synth.stream_id(CONFIG_ID, layer, mi, 1), device="cuda")
                 for pi, (N, M) in enumerate(patterns):
-                    Wp = nm.select(W, a, N, M)
-                    self.packed[(N, M)].append(nm.pack(Wp, N, M))
-                    if pi == 0 and name == "gate_up":
+                    self.packed[(N, M)].append(nm.select_pack(W, a, N, M))
+                    if swiglu and pi == 0 and name == "gate_up":
+                        Wp = nm.select(W, a, N, M)
                         self.swiglu.append(nm.pack_swiglu(Wp[:rows // 2], Wp[rows // 2:], N, M))
-                    if keep_dense and pi == 0:
-                        self.dense.append(Wp)
-                    else:
                         del Wp
+                if keep_dense:
+                    self.dense.append(W)
                 del W, a
         self.io = {}
         for b in batches:
@@ -262,6 +271,25 @@ class Stack:
                     m, v = self.packed[self.patterns[0]][i]
                     ops.append(dict(masks=m, values=v, x=xs[i], y=ys[i], rows=rows, K=K))
                 i += 1
+        return ops
+
+    def qkv_ops(self, batch, pattern, rows_q, rows_k):
+        """The stack with every qkv linear storing q, k and v in three buffers of their own."""
+        _, _, xs, ys = self.io[batch]
+        ops = []
+        for i, (name, rows, K) in enumerate(self.linears()):
+            m, v = self.packed[pattern][i]
+            if name == "qkv":
+                y = ys[i]
+                rows_v = rows - rows_q - rows_k
+                flat = y.view(-1)
+                q = flat[:batch * rows_q].view(batch, rows_q)
+                k = flat[batch * rows_q:batch * (rows_q + rows_k)].view(batch, rows_k)
+                vv = flat[batch * (rows_q + rows_k):].view(batch, rows_v)
+                ops.append(dict(masks=m, values=v, x=xs[i], y=q, y_k=k, y_v=vv, rows=rows, K=K, flags=2,
+                                rows_q=rows_q, rows_k=rows_k))
+            else:
+                ops.append(dict(masks=m, values=v, x=xs[i], y=ys[i], rows=rows, K=K))
         return ops
 
     def dense_ops(self, batch):
@@ -540,6 +568,36 @@ def run_obs_pruning(nm, model, N, M, tokens=2048, repeats=2, cpu=True, linears=s
     return out
 
 
+def time_select_pack(nm, model, pattern, world, layers=1, reps=5):
+    """nm_select_pack (Wanda selection and bitmask pack in one pass) on `layers` decoder
+    layers' linears: ms per layer and the bytes it moves (W read, masks and values written)."""
+    N, M = pattern
+    shapes = [(synth.MODELS[model][n]) for n in synth.MATRICES]
+    Ws, As = [], []
+    for li in range(layers):
+        for mi, (rows, K) in enumerate(shapes):
+            Ws.append(synth.weights(rows, K, 5, synth.stream_id(11, li, mi, 0), device="cuda"))
+            As.append(synth.col_norms(K, 5, synth.stream_id(11, li, mi, 1), device="cuda"))
+    outs = [(torch.empty(W.shape[0], W.shape[1] // 32, dtype=torch.int32, device="cuda"),
+             torch.empty(W.shape[0], W.shape[1] // 2, dtype=torch.bfloat16, device="cuda")) for W in Ws]
+    L = nm.lib()
+
+    def run():
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for W, a, (m, v) in zip(Ws, As, outs):
+            assert L.nm_select_pack(W.data_ptr(), a.data_ptr(), W.shape[0], W.shape[1], N, M, m.data_ptr(),
+                                    v.data_ptr(), s) == 0
+    g = capture(run)
+    t, _ = time_graph(g, reps, 2, world)
+    by = sum(W.numel() * 2 + W.numel() // 8 + W.numel() for W in Ws) + sum(a.numel() * 4 for a in As)
+    peak = measured_peak()[0]
+    del g, Ws, As, outs
+    return {"workload": f"{layers} {model} decoder layer(s): qkv, o, gate_up, down, {N}:{M}",
+            "ms_per_layer": round(t / layers, 4), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
+            "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4),
+            "bytes": f"{by} (W read once; masks and values written)"}
+
+
 def splitk_compare(nm, stack, pattern, world, steps, warmup):
     """The two ways to combine a row block split over CTAs, fp32 output: the
     default deterministic fix-up (the last CTA adds the parts in CTA order) and
@@ -576,6 +634,91 @@ def splitk_compare(nm, stack, pattern, world, steps, warmup):
     return out
 
 
+SUITE = [("qwen3-14b", ((4, 8), (8, 16)), (1,)), ("qwen3-32b", ((4, 8), (8, 16)), (1,)),
+         ("llama3.3-70b", ((2, 4), (16, 32)), (1, 2, 4, 8))]
+
+
+def run_suite(args):
+    """The larger stacks of the pages' Table 3 models, each against its dense references
+    at the same batch. One pattern's packed weights are resident at a time (with the
+    dense weights, the 70B stack needs 137 + 77 GB)."""
+    torch.cuda.set_device(0)
+    import sparse_decoding_gb300 as nm
+    nm.init()
+    peak, peak_kind = measured_peak()
+    steps, warm = args.steps, min(args.warmup, 10)
+    sampler = ClockSampler(0)
+    out = {"metric": METRIC, "unit": UNIT, "peak": {"GB_s": peak, "source": f"{peak_kind} hbm_gbs"}, "models": {}}
+
+    def time_plan(ops, b, dense=False):
+        pl = nm.StackPlan(ops, b, dense=dense)
+        g = capture(pl.run)
+        t, _ = time_graph(g, steps, warm)
+        del g
+        pl.close()
+        return t
+
+    with sampler:
+        for model, pats, batches in SUITE:
+            stack = Stack(nm, model, [pats[0]], batches, args.layers, keep_dense=True, swiglu=False)
+            res = {"layers": stack.layers, "dense": {}, "patterns": {}}
+            for b in batches:
+                dops = stack.dense_ops(b)
+
+                def cublas(dops=dops):
+                    for op in dops:
+                        torch.mm(op["x"], op["W"].t(), out=op["y"])
+                g = capture(cublas)
+                tc, _ = time_graph(g, steps, warm)
+                del g
+                td = time_plan(dops, b, dense=True)
+                res["dense"][f"batch {b}"] = {"hand_written_us": round(td * 1e3, 2), "cublas_us": round(tc * 1e3, 2),
+                                              "GB_s": round(stack.bytes(b, dense=True) / (min(td, tc) * 1e-3) / 1e9, 1)}
+            for pi, pat in enumerate(pats):
+                if pi > 0:  # the next pattern, packed from the same W after the previous one is freed
+                    stack.packed = {pat: []}
+                    torch.cuda.empty_cache()
+                    for i, (name, rows, K) in enumerate(stack.linears()):
+                        layer, mi = divmod(i, 4)
+                        a = synth.col_norms(K, 0, synth.stream_id(CONFIG_ID, layer, mi, 1), device="cuda")
+                        stack.packed[pat].append(nm.select_pack(stack.dense[i], a, *pat))
+                # selection + pack of the whole stack in one pass per linear
+                As = [synth.col_norms(K, 0, synth.stream_id(CONFIG_ID, i // 4, i % 4, 1), device="cuda")
+                      for i, (_, _, K) in enumerate(stack.linears())]
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for i, W in enumerate(stack.dense):
+                    m, v = stack.packed[pat][i]
+                    assert nm.lib().nm_select_pack(W.data_ptr(), As[i].data_ptr(), W.shape[0], W.shape[1], *pat,
+                                                   m.data_ptr(), v.data_ptr(),
+                                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+                e1.record()
+                torch.cuda.synchronize()
+                del As
+                sp_ms = e0.elapsed_time(e1)
+                entry = {"select_pack_ms_whole_stack": round(sp_ms, 2)}
+                for b in batches:
+                    t = time_plan(stack.sparse_ops(pat, b), b)
+                    by = stack.bytes(b)
+                    d = res["dense"][f"batch {b}"]
+                    best = min(d["hand_written_us"], d["cublas_us"])
+                    entry[f"batch {b}"] = {"us_per_token": round(t * 1e3, 2), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
+                                           "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4),
+                                           "ratio_vs_best_dense": round(best / (t * 1e3), 4)}
+                res["patterns"][f"{pat[0]}:{pat[1]}"] = entry
+            shp = synth.MODELS[model]
+            res["workload"] = (f"{model}-shaped decode-token linear stack: {stack.layers} layers x ("
+                               + ", ".join(f"{n} {shp[n][0]}x{shp[n][1]}" for n in synth.MATRICES) + ")")
+            out["models"][model] = res
+            del stack
+            torch.cuda.empty_cache()
+    out["clocks"] = sampler.summary()
+    out["device_status"] = nm.status_str(nm.device_status())
+    out["data"] = "synthetic"
+    print(json.dumps(out), flush=True)
+
+
 def run_ours(args):
     rank, world, local = dist_init()
     torch.cuda.set_device(local)
@@ -585,8 +728,7 @@ def run_ours(args):
     head = (N, M)
     patterns = [head]
     if not args.no_variants:
-        alt = (16, 32) if head != (16, 32) else (2, 4)
-        patterns.append(alt)
+        patterns += [p for p in synth.PATTERNS if p != head]
     batches = [args.batch] + ([] if args.no_variants or args.batch == 4 else [4])
     stack = Stack(nm, args.model, patterns, batches, args.layers, keep_dense=True)
     layers = stack.layers
@@ -648,19 +790,46 @@ def run_ours(args):
         del g
         pl.close()
 
+    def time_plan(ops, b, dense=False):
+        pl = nm.StackPlan(ops, b, dense=dense)
+        g = capture(pl.run)
+        t, _ = time_graph(g, args.steps, min(args.warmup, 10), world)
+        del g
+        pl.close()
+        return t
+
+    def variant_entry(t, b, dense_t=None):
+        by = stack.bytes(b)
+        e = {"us_per_token": round(t * 1e3, 2), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
+             "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4)}
+        if dense_t is not None:
+            e["dense_us_per_token"] = {k: round(v * 1e3, 2) for k, v in dense_t.items()}
+            e["ratio_vs_best_dense"] = round(min(dense_t.values()) / t, 4)
+        return e
+
     variants = {}
     if not args.no_variants:
-        for (pat, b) in [(patterns[-1], B)] + ([(head, 4)] if 4 in stack.io and B != 4 else []):
-            ops = stack.sparse_ops(pat, b)
-            pl = nm.StackPlan(ops, b)
-            g = capture(pl.run)
-            t, _ = time_graph(g, args.steps, min(args.warmup, 10), world)
-            by = stack.bytes(b)
-            variants[f"{pat[0]}:{pat[1]} batch {b}"] = {
-                "us_per_token": round(t * 1e3, 2), "GB_s": round(by / (t * 1e-3) / 1e9, 1),
-                "frac_of_measured_peak": round(by / (t * 1e-3) / 1e9 / peak, 4)}
+        # every pattern at the headline batch (the pages: the same traffic for all four)
+        for pat in patterns[1:]:
+            variants[f"{pat[0]}:{pat[1]} batch {B}"] = variant_entry(time_plan(stack.sparse_ops(pat, B), B), B)
+        # batch 4, with the dense references at batch 4
+        if 4 in stack.io and B != 4:
+            t4 = time_plan(stack.sparse_ops(head, 4), 4)
+            dense4_ops = stack.dense_ops(4)
+            d4 = {"hand_written": time_plan(dense4_ops, 4, dense=True)}
+
+            def cublas4():
+                for op in dense4_ops:
+                    torch.mm(op["x"], op["W"].t(), out=op["y"])
+            g = capture(cublas4)
+            d4["cublas"], _ = time_graph(g, args.steps, min(args.warmup, 10), world)
             del g
-            pl.close()
+            variants[f"{head[0]}:{head[1]} batch 4"] = variant_entry(t4, 4, d4)
+        # q, k and v stored apart (three buffers per qkv linear)
+        rq, rk = synth.QKV_SPLIT[args.model]
+        for b in sorted({B} | ({4} if 4 in stack.io else set())):
+            variants[f"{head[0]}:{head[1]} batch {b}, qkv stored as q, k, v ({rq}/{rk}/{rk} rows)"] = \
+                variant_entry(time_plan(stack.qkv_ops(b, head, rq, rk), b), b)
         # the MLP chained as in a decode layer: gate_up + SwiGLU epilogue -> h -> down
         ops = stack.mlp_ops(B)
         pl = nm.StackPlan(ops, B)
@@ -676,6 +845,9 @@ def run_ours(args):
     split_k = None
     if not args.no_variants:
         split_k = splitk_compare(nm, stack, head, world, max(5, args.steps // 2), min(args.warmup, 5))
+
+    # Wanda selection + pack fused in one pass, for one decoder layer's four linears
+    select_pack = time_select_pack(nm, args.model, head, world)
 
     pruning = None
     if world == 1 and not args.no_pruning:
@@ -729,6 +901,7 @@ def run_ours(args):
         "per_shape": per_shape,
         "variants": variants,
         "split_k_combine": split_k,
+        "select_pack": select_pack,
         "obs_pruning": pruning,
         "e2e": {"value": round(job_us_per_token(e2e_ms, world), 3), "unit": UNIT,
                 "h2d_bytes_per_step": x_all.numel() * 2, "d2h_bytes_per_step": y_all.numel() * 2,
@@ -771,6 +944,9 @@ def main():
         out = run_obs_pruning(nm, args.model, N, M, repeats=args.prune_repeats, cpu=not args.no_cpu_baseline,
                               linears=tuple(args.prune_linears.split(",")))
         print(json.dumps({"obs_pruning": out}), flush=True)
+        return
+    if args.suite:
+        run_suite(args)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -101,6 +101,25 @@ nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K,
                     void *W_pruned, void *stream);
 
 /*
+ * nm_select_pack -- nm_select and nm_pack in one pass over W (the selection
+ * rule of the daiwk.github.io notes, section "核心公式", then the bitmask
+ * conversion of the paper.rainbus.top summary, "方法步骤详情" step 3).
+ *   W_bf16 : device, bf16 [rows][K], the dense weights (read).
+ *   a      : device, fp32 [K], the per-column activation norm (read).
+ *   masks, values_bf16 : device (written), as nm_pack writes them for the
+ *            matrix nm_select would return.
+ * (N, M) must be a 50% pattern (NM_ERR_UNSUPPORTED otherwise). The result is
+ * bit-identical with nm_select followed by nm_pack, without the pruned matrix
+ * being written and read back. The mask word is the selection's keep mask,
+ * except where a kept weight is zero and outranks a lower-index zero (possible
+ * only with a NaN or infinite column norm), where the pack's fill rule
+ * decides. It cannot be NM_ERR_NOT_NM: the rule keeps N per subgroup.
+ * Asynchronous.
+ */
+nm_status nm_select_pack(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
+                         void *values_bf16, void *stream);
+
+/*
  * nm_pack -- bitmask conversion on the GPU, bit-exact with nm_pack_host.
  *   W_bf16 : device, bf16 [rows][K] (read). masks, values_bf16: device (written).
  * Synchronous with respect to `stream`: it waits for the stream so that it can
@@ -169,22 +188,30 @@ typedef struct nm_linear {
     const void *values; /* bf16 [rows][K/2] */
     const void *W;      /* bf16 [rows][K] */
     const void *x;      /* bf16 [batch][K] */
-    void *y;            /* bf16 [batch][rows] ([batch][rows/2] with NM_LINEAR_SWIGLU) */
+    void *y;            /* bf16 [batch][rows] ([batch][rows/2] with NM_LINEAR_SWIGLU;
+                           the q part [batch][rows_q] with NM_LINEAR_QKV) */
     int64_t rows;
     int64_t K;
-    uint32_t flags;     /* 0, or NM_LINEAR_SWIGLU (sparse ops only) */
+    uint32_t flags;     /* 0, NM_LINEAR_SWIGLU or NM_LINEAR_QKV (sparse ops only) */
+    void *y_k;          /* NM_LINEAR_QKV: bf16 [batch][rows_k]; unused otherwise */
+    void *y_v;          /* NM_LINEAR_QKV: bf16 [batch][rows - rows_q - rows_k]; unused otherwise */
+    int64_t rows_q;     /* NM_LINEAR_QKV: rows of the q and k parts; unused otherwise */
+    int64_t rows_k;
 } nm_linear;
 
 /* The op is a gate/up pair matrix in the pair layout of nm_pack_swiglu
  * (rows = 2 * rows_h, a multiple of 32) and stores h as nm_spmv_swiglu does. */
 #define NM_LINEAR_SWIGLU 1u
+/* The op stores its rows in three buffers (y, y_k, y_v) as nm_spmv_qkv does. */
+#define NM_LINEAR_QKV 2u
 
 /*
  * nm_spmv_stack / dense_gemv_stack -- the linear stack of one decode token
  * (every pruned linear of every layer; only linear layers are sparse, per the
  * ai.info summary, "Methodology" step 4 and paper.rainbus.top "局限与改进").
  * Runs ops[0..n_ops) in order on `stream`, each as nm_spmv / dense_gemv (an op
- * with NM_LINEAR_SWIGLU as nm_spmv_swiglu; dense ops take flags 0).
+ * with NM_LINEAR_SWIGLU as nm_spmv_swiglu, one with NM_LINEAR_QKV as
+ * nm_spmv_qkv; dense ops take flags 0).
  * Consecutive launches are chained with programmatic dependent launch: a
  * kernel may start streaming its own weights before the previous one ends,
  * but reads its x only after the previous kernel has completed, exactly as if
@@ -219,6 +246,24 @@ nm_status nm_pack_swiglu(const void *W_gate_bf16, const void *W_up_bf16, int64_t
                          uint32_t *masks, void *values_bf16, void *stream);
 nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *h_bf16,
                          int64_t rows_h, int64_t K, int batch, void *stream);
+
+/*
+ * nm_spmv_qkv -- nm_spmv of a fused q/k/v projection whose output goes to
+ * three buffers, one per projection, so that each is contiguous per token at
+ * any batch size (the step after the SpMV in a decode layer's attention
+ * block; the pages prune only the linear layers: ai.info summary,
+ * "Methodology in Plain English" step 4).
+ *   masks, values_bf16: the packed matrix of rows_q + rows_k + rows_v rows
+ *     (the q rows, then the k rows, then the v rows); x_bf16: [batch][K].
+ *   q_bf16 [batch][rows_q], k_bf16 [batch][rows_k], v_bf16 [batch][rows_v]:
+ *     device bf16 (written); row r of the product goes to q when r < rows_q,
+ *     to k row r - rows_q when r < rows_q + rows_k, else to v row
+ *     r - rows_q - rows_k. Values and summation order are nm_spmv's.
+ * A part with no rows may be NULL. Errors and the rest as for nm_spmv
+ * (NM_ERR_SHAPE for a negative row count). Asynchronous.
+ */
+nm_status nm_spmv_qkv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *q_bf16, void *k_bf16,
+                      void *v_bf16, int64_t rows_q, int64_t rows_k, int64_t rows_v, int64_t K, int batch, void *stream);
 
 /*
  * nm_stack_plan -- a decode-token stack prepared once, run many times.
@@ -282,20 +327,26 @@ nm_status nm_stack_plan_destroy(nm_stack_plan *plan);
  *   The first call on a device looks up the array's device address (with that
  *   device current); make that first call outside CUDA graph capture.
  *   Every call on a device shares the one array and finds it as the previous
- *   call left it; each call clears the counters it needs at its start. Calls
- *   whose executions overlap on the GPU (other streams, or other host threads)
- *   race on the array: serialize them. A bounded wait that runs out is not
- *   reported by nm_device_status for this call.
+ *   call left it; each call clears the counters it needs at its start (one
+ *   2 KB cudaMemsetAsync on `stream` before the kernel). Calls whose
+ *   executions overlap on the GPU (other streams, or other host threads) race
+ *   on the array: serialize them. A bounded wait that runs out is reported by
+ *   nm_device_status (below), which reads and clears the array's status word
+ *   as well as the library scratch's.
  */
 nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const void *x_bf16,
                           void *y_bf16, int64_t rows, int64_t K, int batch, void *stream);
 
 /*
  * nm_device_status -- waits for `stream`, then returns and clears the status
- * word of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
- * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed). After
- * a timeout it also clears the scratch's stream-K counters (outputs of the
- * calls that ran meanwhile are unspecified); call it before reusing the device.
+ * words of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
+ * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed). It
+ * covers the library scratch and, once nm_spmv_noalloc has run on the device,
+ * that call's static array. After a timeout it also clears the stream-K
+ * counters (outputs of the calls that ran meanwhile are unspecified); call it
+ * before reusing the device. It allocates the library scratch if that does not
+ * exist yet -- except on a device where only nm_spmv_noalloc has run, where it
+ * reads that call's array alone and allocates nothing.
  */
 nm_status nm_device_status(void *stream);
 

@@ -33,6 +33,7 @@ PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 NM_STACK_DENSE = 1
 NM_STACK_PERSISTENT = 2
 NM_LINEAR_SWIGLU = 1
+NM_LINEAR_QKV = 2
 NM_OBS_SGEMM = 1
 
 # Every symbol the header declares (the CPU test checks they are exported).
@@ -40,7 +41,7 @@ EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_p
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
            "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
            "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu", "nm_obs_hessian", "nm_obs_prune",
-           "nm_spmv_f32out_atomic")
+           "nm_spmv_f32out_atomic", "nm_select_pack", "nm_spmv_qkv")
 
 
 class NmError(RuntimeError):
@@ -53,7 +54,8 @@ class NmLinear(ctypes.Structure):
     """Mirror of ``nm_linear`` in include/nmspmv.h."""
     _fields_ = [("masks", ctypes.c_void_p), ("values", ctypes.c_void_p), ("W", ctypes.c_void_p),
                 ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("K", ctypes.c_int64), ("flags", ctypes.c_uint32)]
+                ("K", ctypes.c_int64), ("flags", ctypes.c_uint32), ("y_k", ctypes.c_void_p),
+                ("y_v", ctypes.c_void_p), ("rows_q", ctypes.c_int64), ("rows_k", ctypes.c_int64)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -75,9 +77,11 @@ def lib() -> ctypes.CDLL:
         "nm_pack_host": ([p, i64, i64, i32, i32, p, p], i32),
         "nm_select": ([p, p, i64, i64, i32, i32, p, p], i32),
         "nm_pack": ([p, i64, i64, i32, i32, p, p, p], i32),
+        "nm_select_pack": ([p, p, i64, i64, i32, i32, p, p, p], i32),
         "nm_spmv": ([p, p, p, p, i64, i64, i32, p], i32),
         "nm_spmv_f32out": ([p, p, p, p, i64, i64, i32, p], i32),
         "nm_spmv_f32out_atomic": ([p, p, p, p, i64, i64, i32, p], i32),
+        "nm_spmv_qkv": ([p, p, p, p, p, p, i64, i64, i64, i64, i32, p], i32),
         "dense_gemv": ([p, p, p, i64, i64, i32, p], i32),
         "dense_gemv_f32out": ([p, p, p, i64, i64, i32, p], i32),
         "nm_spmv_stack": ([ctypes.POINTER(NmLinear), i32, i32, p], i32),
@@ -152,6 +156,19 @@ def select(W: torch.Tensor, a: torch.Tensor, N: int, M: int, out: Optional[torch
     return out
 
 
+def select_pack(W: torch.Tensor, a: torch.Tensor, N: int, M: int):
+    """Wanda N:M selection and pack in one pass: dense W (bf16, CUDA) and column norms a (fp32)
+    -> (masks int32-viewed uint32 [rows][K/32], values bf16 [rows][K/2]); equal to pack(select(W, a))."""
+    _cuda(W, torch.bfloat16, "W")
+    _cuda(a, torch.float32, "a")
+    rows, K = W.shape
+    masks = torch.empty(rows, K // 32, dtype=torch.int32, device=W.device)
+    values = torch.empty(rows, K // 2, dtype=torch.bfloat16, device=W.device)
+    _check(lib().nm_select_pack(W.data_ptr(), a.data_ptr(), rows, K, N, M, masks.data_ptr(), values.data_ptr(),
+                                ctypes.c_void_p(_stream(W))), "nm_select_pack")
+    return masks, values
+
+
 def pack(W: torch.Tensor, N: int, M: int):
     """Pruned dense W (bf16, CUDA) -> (masks int32-viewed uint32 [rows][K/32], values bf16 [rows][K/2])."""
     _cuda(W, torch.bfloat16, "W")
@@ -196,6 +213,28 @@ def spmv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, out: Option
     _check(getattr(lib(), name)(masks.data_ptr(), values.data_ptr(), x.data_ptr(), out.data_ptr(), rows, K, batch,
                                 ctypes.c_void_p(_stream(x))), name)
     return out
+
+
+def spmv_qkv(masks: torch.Tensor, values: torch.Tensor, x: torch.Tensor, rows_q: int, rows_k: int,
+             out: Optional[Sequence[torch.Tensor]] = None):
+    """The SpMV of a fused q/k/v matrix (q rows, then k rows, then v rows) into three bf16
+    buffers q [batch][rows_q], k [batch][rows_k], v [batch][rows_v]; returns (q, k, v)."""
+    _cuda(masks, torch.int32, "masks")
+    _cuda(values, torch.bfloat16, "values")
+    x = _cuda(_x2d(x), torch.bfloat16, "x")
+    rows = masks.shape[0]
+    K = masks.shape[1] * 32
+    batch = x.shape[0]
+    rows_v = rows - rows_q - rows_k
+    if values.shape != (rows, K // 2) or x.shape[1] != K or rows_q < 0 or rows_k < 0 or rows_v < 0:
+        raise ValueError("shape mismatch between masks, values, x and the q/k/v row counts")
+    if out is None:
+        out = [torch.empty(batch, r, dtype=torch.bfloat16, device=x.device) for r in (rows_q, rows_k, rows_v)]
+    q, k, v = (_cuda(t, torch.bfloat16, n) for t, n in zip(out, ("q", "k", "v")))
+    _check(lib().nm_spmv_qkv(masks.data_ptr(), values.data_ptr(), x.data_ptr(), q.data_ptr(), k.data_ptr(),
+                             v.data_ptr(), rows_q, rows_k, rows_v, K, batch, ctypes.c_void_p(_stream(x))),
+           "nm_spmv_qkv")
+    return q, k, v
 
 
 def pack_swiglu(W_gate: torch.Tensor, W_up: torch.Tensor, N: int, M: int):
@@ -258,6 +297,11 @@ def _linear_array(ops: Sequence[dict]) -> ctypes.Array:
         t.rows = int(op["rows"])
         t.K = int(op["K"])
         t.flags = int(op.get("flags", 0))
+        for f in ("y_k", "y_v"):
+            v = op.get(f)
+            setattr(t, f, v.data_ptr() if v is not None else None)
+        t.rows_q = int(op.get("rows_q", 0))
+        t.rows_k = int(op.get("rows_k", 0))
     return arr
 
 

@@ -98,10 +98,25 @@ static nm_status check_gemv_args(const void *W, const void *x, const void *y, in
     return NM_OK;
 }
 
+// The three output parts of nm_spmv_qkv: row counts and buffers.
+static nm_status check_qkv_parts(const void *q, const void *k, const void *v, int64_t rows_q, int64_t rows_k,
+                                 int64_t rows_v)
+{
+    if (rows_q < 0 || rows_k < 0 || rows_v < 0)
+        return NM_ERR_SHAPE;
+    if ((rows_q > 0 && !q) || (rows_k > 0 && !k) || (rows_v > 0 && !v))
+        return NM_ERR_INVALID_ARG;
+    if ((rows_q > 0 && !aligned16(q)) || (rows_k > 0 && !aligned16(k)) || (rows_v > 0 && !aligned16(v)))
+        return NM_ERR_ALIGN;
+    return NM_OK;
+}
+
 // One op of a stack: the checks of its call, and its flags.
 static nm_status check_stack_op(const nm_linear &o, bool dense, int batch)
 {
-    if (o.flags & ~(uint32_t)NM_LINEAR_SWIGLU)
+    if (o.flags & ~(uint32_t)(NM_LINEAR_SWIGLU | NM_LINEAR_QKV))
+        return NM_ERR_INVALID_ARG;
+    if ((o.flags & NM_LINEAR_SWIGLU) && (o.flags & NM_LINEAR_QKV))
         return NM_ERR_INVALID_ARG;
     if (dense) {
         if (o.flags)
@@ -110,8 +125,29 @@ static nm_status check_stack_op(const nm_linear &o, bool dense, int batch)
     }
     if ((o.flags & NM_LINEAR_SWIGLU) && o.rows % 32 != 0)
         return NM_ERR_SHAPE;
+    if (o.flags & NM_LINEAR_QKV) {
+        const int64_t rows_v = o.rows - o.rows_q - o.rows_k;
+        nm_status s = check_qkv_parts(o.y, o.y_k, o.y_v, o.rows_q, o.rows_k, rows_v);
+        if (s != NM_OK)
+            return s;
+        if (o.rows == 0)
+            return NM_OK;
+        if (o.K > 0 && (!o.masks || !o.values || !o.x))
+            return NM_ERR_INVALID_ARG;
+        if (o.K > 0 && (!aligned16(o.masks) || !aligned16(o.values) || !aligned16(o.x)))
+            return NM_ERR_ALIGN;
+        return (o.K < 0 || o.K % 32 != 0) ? NM_ERR_SHAPE : (batch < 1 || batch > 8) ? NM_ERR_UNSUPPORTED : NM_OK;
+    }
     return check_spmv_args(o.masks, o.values, o.x, o.y, o.rows, o.K, batch);
 }
+
+// The output parts of a kOutQkv launch.
+struct QkvOut {
+    void *y_k = nullptr;
+    void *y_v = nullptr;
+    int64_t rows_q = 0;
+    int64_t rows_k = 0;
+};
 
 static nm_status zero_output(void *y, int64_t rows, int batch, size_t elt, cudaStream_t stream)
 {
@@ -120,20 +156,48 @@ static nm_status zero_output(void *y, int64_t rows, int batch, size_t elt, cudaS
 
 // out: kOutBf16, kOutF32, or kOutSwiglu (rows = gate/up pair rows, y = h [batch][rows / 2]).
 static nm_status spmv_impl(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
-                           int64_t K, int batch, cudaStream_t stream, bool pdl, bool splitk_atomic = false)
+                           int64_t K, int batch, cudaStream_t stream, bool pdl, bool splitk_atomic = false,
+                           const QkvOut *qkv = nullptr)
 {
-    nm_status s = check_spmv_args(masks, values, x, y, rows, K, batch);
-    if (s != NM_OK || rows == 0)
+    nm_status s;
+    if (out == kOutQkv) { // y is the q part and may be NULL when it has no rows: checked by the caller
+        if (rows < 0 || K < 0 || (K % 32) != 0)
+            return NM_ERR_SHAPE;
+        if (batch < 1 || batch > 8)
+            return NM_ERR_UNSUPPORTED;
+        if (rows == 0)
+            return NM_OK;
+        if (K > 0 && (!masks || !values || !x))
+            return NM_ERR_INVALID_ARG;
+        if (K > 0 && (!aligned16(masks) || !aligned16(values) || !aligned16(x)))
+            return NM_ERR_ALIGN;
+    } else if ((s = check_spmv_args(masks, values, x, y, rows, K, batch)) != NM_OK || rows == 0) {
         return s;
+    }
     if (out == kOutSwiglu && rows % 32 != 0)
         return NM_ERR_SHAPE;
-    if (K == 0)
+    if (K == 0) {
+        if (out == kOutQkv) {
+            const int64_t rows_v = rows - qkv->rows_q - qkv->rows_k;
+            if ((qkv->rows_q > 0 && (s = zero_output(y, qkv->rows_q, batch, 2, stream)) != NM_OK) ||
+                (qkv->rows_k > 0 && (s = zero_output(qkv->y_k, qkv->rows_k, batch, 2, stream)) != NM_OK) ||
+                (rows_v > 0 && (s = zero_output(qkv->y_v, rows_v, batch, 2, stream)) != NM_OK))
+                return s;
+            return NM_OK;
+        }
         return out == kOutSwiglu ? zero_output(y, rows / 2, batch, 2, stream)
                                  : zero_output(y, rows, batch, out == kOutF32 ? 4 : 2, stream);
+    }
     LaunchCtx ctx;
     if ((s = device_ctx(stream, pdl, &ctx)) != NM_OK)
         return s;
     ctx.splitk_atomic = splitk_atomic;
+    if (qkv) {
+        ctx.y_k = qkv->y_k;
+        ctx.y_v = qkv->y_v;
+        ctx.rows_q = qkv->rows_q;
+        ctx.rows_k = qkv->rows_k;
+    }
     s = launch_spmv(masks, values, x, y, out, rows, K, batch, ctx);
     if (s == NM_OK && cudaGetLastError() != cudaSuccess)
         s = NM_ERR_CUDA;
@@ -240,7 +304,7 @@ static void capture_chain(nm_stack_plan *pl)
 
 extern "C" {
 
-int nm_abi_version(void) { return 3; }
+int nm_abi_version(void) { return 4; }
 
 const char *nm_status_str(int status)
 {
@@ -276,6 +340,26 @@ nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K,
     if (s != NM_OK)
         return s;
     return launch_select(W_bf16, a, rows, K, N, M, W_pruned, ctx);
+}
+
+nm_status nm_select_pack(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
+                         void *values_bf16, void *stream)
+{
+    if (!pattern_ok(N, M))
+        return NM_ERR_UNSUPPORTED;
+    if (rows < 0 || K < 0 || (K % 32) != 0)
+        return NM_ERR_SHAPE;
+    if (rows == 0 || K == 0)
+        return NM_OK;
+    if (!W_bf16 || !a || !masks || !values_bf16)
+        return NM_ERR_INVALID_ARG;
+    if (!aligned16(W_bf16) || !aligned16(a) || !aligned16(masks) || !aligned16(values_bf16))
+        return NM_ERR_ALIGN;
+    LaunchCtx ctx;
+    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    return launch_select_pack(W_bf16, a, rows, K, N, M, masks, values_bf16, ctx);
 }
 
 nm_status nm_pack(const void *W_bf16, int64_t rows, int64_t K, int N, int M, uint32_t *masks, void *values_bf16,
@@ -315,6 +399,21 @@ nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const v
     return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false);
 }
 
+nm_status nm_spmv_qkv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *q_bf16, void *k_bf16,
+                      void *v_bf16, int64_t rows_q, int64_t rows_k, int64_t rows_v, int64_t K, int batch, void *stream)
+{
+    nm_status s = check_qkv_parts(q_bf16, k_bf16, v_bf16, rows_q, rows_k, rows_v);
+    if (s != NM_OK)
+        return s;
+    QkvOut qo;
+    qo.y_k = k_bf16;
+    qo.y_v = v_bf16;
+    qo.rows_q = rows_q;
+    qo.rows_k = rows_k;
+    return spmv_impl(masks, values_bf16, x_bf16, q_bf16, kOutQkv, rows_q + rows_k + rows_v, K, batch,
+                     (cudaStream_t)stream, false, false, &qo);
+}
+
 nm_status nm_spmv_f32out_atomic(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
                                 int64_t rows, int64_t K, int batch, void *stream)
 {
@@ -343,9 +442,15 @@ nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream
             return s;
     }
     for (int i = 0; i < n_ops; ++i) {
-        nm_status s = spmv_impl(ops[i].masks, ops[i].values, ops[i].x, ops[i].y,
-                                (ops[i].flags & NM_LINEAR_SWIGLU) ? kOutSwiglu : kOutBf16, ops[i].rows, ops[i].K, batch,
-                                (cudaStream_t)stream, true);
+        const nm_linear &o = ops[i];
+        QkvOut qo;
+        qo.y_k = o.y_k;
+        qo.y_v = o.y_v;
+        qo.rows_q = o.rows_q;
+        qo.rows_k = o.rows_k;
+        const int out = (o.flags & NM_LINEAR_SWIGLU) ? kOutSwiglu : (o.flags & NM_LINEAR_QKV) ? kOutQkv : kOutBf16;
+        nm_status s = spmv_impl(o.masks, o.values, o.x, o.y, out, o.rows, o.K, batch, (cudaStream_t)stream, true, false,
+                                out == kOutQkv ? &qo : nullptr);
         if (s != NM_OK)
             return s;
     }
@@ -490,26 +595,48 @@ nm_status nm_stack_plan_destroy(nm_stack_plan *plan)
     return s;
 }
 
-nm_status nm_device_status(void *stream)
+// Read and clear a scratch's status word on `st`; after a timeout also clear
+// its stream-K counters (a kernel that gave up may have left them mid-count).
+static nm_status read_clear_status(const Scratch &sc, size_t counter_bytes, cudaStream_t st)
 {
-    LaunchCtx ctx;
-    nm_status s = device_ctx((cudaStream_t)stream, false, &ctx);
-    if (s != NM_OK)
-        return s;
-    cudaStream_t st = (cudaStream_t)stream;
     uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, ctx.scratch.status, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaMemsetAsync(ctx.scratch.status, 0, sizeof word, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
+    if (cudaMemcpyAsync(&word, sc.status, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(sc.status, 0, sizeof word, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
     if (!(word & (1u << NM_ERR_TIMEOUT)))
         return NM_OK;
-    // A kernel that gave up may have left the stream-K counters mid-count:
-    // clear them, so that later calls start from a clean state.
-    if (cudaMemsetAsync(ctx.scratch.counters, 0, kScratchCounterBytes, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
+    if (cudaMemsetAsync(sc.counters, 0, counter_bytes, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_ERR_TIMEOUT;
+}
+
+nm_status nm_device_status(void *stream)
+{
+    cudaStream_t st = (cudaStream_t)stream;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return NM_ERR_CUDA;
+    // nm_spmv_noalloc's static scratch, if a call has set it up on this device
+    Scratch na;
+    nm_status s_na = NM_OK;
+    const bool have_na = noalloc_scratch(dev, &na);
+    if (have_na && (s_na = read_clear_status(na, kScratchCounterBytes, st)) == NM_ERR_CUDA)
+        return s_na;
+    bool have_lib;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        have_lib = g_scratch[dev] != nullptr;
+    }
+    if (have_na && !have_lib)
+        return s_na; // allocate nothing for a caller that only uses nm_spmv_noalloc
+    LaunchCtx ctx;
+    nm_status s = device_ctx(st, false, &ctx);
+    if (s != NM_OK)
+        return s;
+    s = read_clear_status(ctx.scratch, kScratchCounterBytes, st);
+    if (s == NM_OK)
+        s = s_na;
+    return s;
 }
 
 } // extern "C"

@@ -18,6 +18,11 @@ struct LaunchCtx {
     // Split K over every CTA slot and add the parts of a shared row block with
     // fp32 atomicAdd into y (fp32 output only; the launcher zeroes y first).
     bool splitk_atomic = false;
+    // kOutQkv: rows [0, rows_q) go to y, [rows_q, rows_q + rows_k) to y_k, the rest to y_v.
+    void *y_k = nullptr;
+    void *y_v = nullptr;
+    int64_t rows_q = 0;
+    int64_t rows_k = 0;
 };
 
 // Which kernel nm_spmv uses for a shape (exposed for tests and tooling).
@@ -29,7 +34,8 @@ int spmv_max_ctas(int num_sms);
 
 // What the SpMV stores: y in bf16, y in fp32, or (gate/up row pairs, see
 // nm_spmv_swiglu) h = silu(gate) * up in bf16.
-enum OutMode { kOutBf16 = 0, kOutF32 = 1, kOutSwiglu = 2 };
+// kOutQkv: bf16 y split by rows into three buffers (see nm_spmv_qkv).
+enum OutMode { kOutBf16 = 0, kOutF32 = 1, kOutSwiglu = 2, kOutQkv = 3 };
 
 nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, void *y, int out, int64_t rows,
                       int64_t K, int batch, const LaunchCtx &ctx);
@@ -37,6 +43,8 @@ nm_status launch_gemv(const void *W, const void *x, void *y, bool f32out, int64_
                       int batch, const LaunchCtx &ctx);
 nm_status launch_select(const void *W, const float *a, int64_t rows, int64_t K, int N, int M,
                         void *out, const LaunchCtx &ctx);
+nm_status launch_select_pack(const void *W, const float *a, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
+                             void *values, const LaunchCtx &ctx);
 // pair_off < 0: row r of W is row r of the output; 0 / 16: row r goes to
 // (r / 16) * 32 + r % 16 + pair_off (the gate / up half of the pair layout).
 nm_status launch_pack(const void *W, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
@@ -58,6 +66,10 @@ nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t
                               const LaunchCtx &ctx);
 nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
                              const LaunchCtx &ctx);
+
+// The static scratch of nm_spmv_noalloc on device `dev`, if a call has set it
+// up there (noalloc.cu).
+bool noalloc_scratch(int dev, Scratch *out);
 
 // Returns the driver's cuTensorMapEncodeTiled, or nullptr if unavailable.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

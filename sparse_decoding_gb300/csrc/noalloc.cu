@@ -53,6 +53,19 @@ static nm_status noalloc_setup(int dev, void **ptr, int *sms)
     return NM_OK;
 }
 
+// For nm_device_status: the array's status word and counters on this device
+// if a call has set it up there (no lookup otherwise: nothing to report).
+bool noalloc_scratch(int dev, Scratch *out)
+{
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return false;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev])
+        return false;
+    *out = scratch_from_base(g_noalloc_ptr[dev]);
+    return true;
+}
+
 } // namespace nm
 
 extern "C" nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const void *x_bf16,

@@ -328,8 +328,9 @@ template <int B> struct SparseCfg {
 template <int B, int OUT>
 __global__ void __launch_bounds__(256)
     spmv_simple_kernel(const uint32_t *__restrict__ masks, const uint16_t *__restrict__ values,
-                       const uint16_t *__restrict__ x, void *y, int64_t rows, int64_t K)
+                       const uint16_t *__restrict__ x, const StreamKParams out, int64_t K)
 {
+    const int64_t rows = out.rows;
     pdl_wait_upstream();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(256)
                 }
             }
         }
-        store_y<B, OUT>(y, rows, row, acc);
+        store_y<B, OUT>(out, row, acc);
     }
 }
 
@@ -441,8 +442,15 @@ static nm_status launch_simple(const uint32_t *masks, const void *values, const 
     attr[0].val.programmaticStreamSerializationAllowed = ctx.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    StreamKParams out = {}; // the output fields only
+    out.y = y;
+    out.rows = rows;
+    out.y_k = ctx.y_k;
+    out.y_v = ctx.y_v;
+    out.rows_q = ctx.rows_q;
+    out.rows_qk = ctx.rows_q + ctx.rows_k;
     if (cudaLaunchKernelEx(&cfg, spmv_simple_kernel<B, OUT>, masks, (const uint16_t *)values,
-                           (const uint16_t *)x, y, rows, K) != cudaSuccess)
+                           (const uint16_t *)x, out, K) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_OK;
 }
@@ -509,6 +517,7 @@ nm_status launch_spmv(const uint32_t *masks, const void *values, const void *x, 
     case kOutBf16: return dispatch<kOutBf16>(masks, values, x, y, rows, K, batch, ctx);
     case kOutF32: return dispatch<kOutF32>(masks, values, x, y, rows, K, batch, ctx);
     case kOutSwiglu: return dispatch<kOutSwiglu>(masks, values, x, y, rows, K, batch, ctx);
+    case kOutQkv: return dispatch<kOutQkv>(masks, values, x, y, rows, K, batch, ctx);
     default: return NM_ERR_INVALID_ARG;
     }
 }

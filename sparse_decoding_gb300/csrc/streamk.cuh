@@ -71,6 +71,10 @@ struct StreamKParams {
     int32_t pair_k;       // CTA pairs (clusters of 2) split each row block's K in halves (see queue_finish_pair)
     uint32_t kc_inv;      // ceil(2^32 / KC): n / KC = umulhi(n, kc_inv) for the small n used
     int32_t atomic;       // parts of a shared row block go to y by fp32 atomicAdd (y zeroed before)
+    void *y_k;            // kOutQkv: the buffers of rows [rows_q, rows_qk) and [rows_qk, rows)
+    void *y_v;
+    int64_t rows_q;
+    int64_t rows_qk;
     Scratch scratch;
 };
 
@@ -87,9 +91,36 @@ template <class Pol, int B, int W, int NBUF> constexpr int queue_bytes()
 // row block t hold gate rows 16t..16t+15, lanes 16-31 the up rows of the same
 // indices -- and lane i < 16 stores h[16t + i] = bf16_rn(silu(g) * u) with
 // silu(g) = g / (1 + exp(-g)), all in fp32; y is then h [batch][rows / 2].
+// kOutQkv: row r goes to the one of three [batch][part rows] buffers whose
+// row range holds it (q: [0, rows_q), k: [rows_q, rows_qk), v: the rest).
 template <int B, int OUT>
-__device__ __forceinline__ void store_y(void *y, int64_t rows, int64_t row, const float (&v)[B])
+__device__ __forceinline__ void store_y(const StreamKParams &p, int64_t row, const float (&v)[B])
 {
+    void *const y = p.y;
+    const int64_t rows = p.rows;
+    if constexpr (OUT == kOutQkv) {
+        if (row >= rows)
+            return;
+        uint16_t *dst;
+        int64_t n, r;
+        if (row < p.rows_q) {
+            dst = (uint16_t *)y;
+            n = p.rows_q;
+            r = row;
+        } else if (row < p.rows_qk) {
+            dst = (uint16_t *)p.y_k;
+            n = p.rows_qk - p.rows_q;
+            r = row - p.rows_q;
+        } else {
+            dst = (uint16_t *)p.y_v;
+            n = rows - p.rows_qk;
+            r = row - p.rows_qk;
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+            dst[(int64_t)b * n + r] = f32_to_bf16_rn(v[b]);
+        return;
+    }
     if constexpr (OUT == kOutSwiglu) {
         const int lane = (int)(row & 31);
         const int64_t hrows = rows >> 1, hr = (row >> 5) * 16 + lane;
@@ -153,7 +184,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
     const int64_t rb_lo = rb * KC, rb_hi = rb_lo + KC;
     const int64_t row = rb * kUnitRows + lane;
     if (rb_lo >= cr.cs && rb_hi <= cr.ce) {
-        store_y<B, OUT>(p.y, p.rows, row, tot);
+        store_y<B, OUT>(p, row, tot);
         return;
     }
     if constexpr (OUT == kOutF32) {
@@ -213,7 +244,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
             for (int b = 0; b < B; ++b)
                 sum[b] += v[j][b];
     }
-    store_y<B, OUT>(p.y, p.rows, row, sum);
+    store_y<B, OUT>(p, row, sum);
     if (lane == 0)
         atomicExch(&p.scratch.counters[first], 0u);
 }
@@ -462,7 +493,7 @@ __device__ __forceinline__ void consume_range(const TensorMaps *maps, const Stre
                     acc[q][b] = 0.f;
             }
             if (seg_kc0 == 0 && kc + 1 == KC) {
-                store_y<B, OUT>(p.y, p.rows, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
+                store_y<B, OUT>(p, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
             } else {
                 float *mine = part + ((warp * 2 + (rb == w.rb0 ? 0 : 1)) * B) * 32 + lane;
 #pragma unroll
@@ -702,7 +733,7 @@ __device__ __forceinline__ void queue_finish_pair(const StreamKParams &p, const 
     if (warp == 0 && rank == 0 && cr.ce > cr.cs) {
         float v[B];
         v[0] = tot + qv.peer[lane];
-        store_y<B, OUT>(p.y, p.rows, div64(cr.cs, p.KC) * kUnitRows + lane, v);
+        store_y<B, OUT>(p, div64(cr.cs, p.KC) * kUnitRows + lane, v);
     }
 }
 
@@ -808,6 +839,8 @@ __device__ __forceinline__ StreamKParams op_params(const StackOp *op, const Scra
     p.pair_k = 0;
     p.kc_inv = 0;
     p.atomic = 0;
+    p.y_k = p.y_v = nullptr;
+    p.rows_q = p.rows_qk = 0;
     p.scratch = scratch;
     return p;
 }
@@ -999,6 +1032,10 @@ nm_status launch_streamk(const TensorMaps &maps, void *y, int64_t rows, int64_t 
     p.y = y;
     p.rows = rows;
     p.KC = (int32_t)KC;
+    p.y_k = ctx.y_k;
+    p.y_v = ctx.y_v;
+    p.rows_q = ctx.rows_q;
+    p.rows_qk = ctx.rows_q + ctx.rows_k;
     p.U = ((rows + kUnitRows - 1) / kUnitRows) * KC;
     p.scratch = ctx.scratch;
     const int64_t nrb = (rows + kUnitRows - 1) / kUnitRows;

@@ -128,6 +128,11 @@ MODELS = {"llama3.1-8b": LLAMA31_8B, "qwen3-14b": QWEN3_14B, "qwen3-32b": QWEN3_
 
 PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 
+# Rows of the q and of the k projection inside each model's fused qkv matrix
+# (q rows first, then k, then v with as many rows as k).
+QKV_SPLIT = {"llama3.1-8b": (4096, 1024), "qwen3-14b": (5120, 1024), "qwen3-32b": (8192, 1024),
+             "llama3.3-70b": (8192, 1024)}
+
 
 def calibration(T: int, K: int, seed: int = 0, stream: int = 5, dead=(), device="cpu") -> torch.Tensor:
     """Calibration inputs X for one linear layer, bf16 ``[T][K]`` (token-major).

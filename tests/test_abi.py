@@ -40,11 +40,16 @@ def test_header_declares_the_abi():
 
 
 def test_linear_struct_matches_header(nm):
-    """nm_linear: five pointers, two int64, one uint32 (padded to 8 bytes)."""
-    assert ctypes.sizeof(nm.NmLinear) == 5 * 8 + 2 * 8 + 8
-    assert nm.lib().nm_abi_version() == 3
+    """nm_linear: five pointers, two int64, one uint32 (padded to 8 bytes), then the
+    q/k/v split fields: two pointers, two int64."""
+    assert ctypes.sizeof(nm.NmLinear) == 5 * 8 + 2 * 8 + 8 + 2 * 8 + 2 * 8
+    assert nm.NmLinear.y_k.offset == 64 and nm.NmLinear.rows_k.offset == 88
+    assert nm.lib().nm_abi_version() == 4
     text = open(HEADER).read()
-    assert "uint32_t flags;" in text and "#define NM_LINEAR_SWIGLU 1u" in text
+    assert "uint32_t flags;" in text and "#define NM_LINEAR_SWIGLU 1u" in text and "#define NM_LINEAR_QKV 2u" in text
+    body = text[text.index("typedef struct nm_linear {"):text.index("} nm_linear;")]
+    fields = re.findall(r"(\w+);", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+    assert fields == ["masks", "values", "W", "x", "y", "rows", "K", "flags", "y_k", "y_v", "rows_q", "rows_k"], fields
 
 
 def test_library_exports_every_declared_symbol(nm):
@@ -52,7 +57,7 @@ def test_library_exports_every_declared_symbol(nm):
     for name in declared_functions():
         assert hasattr(L, name), f"libnmspmv.so does not export {name}"
     assert set(declared_functions()) <= set(nm.EXPORTS), set(declared_functions()) - set(nm.EXPORTS)
-    assert L.nm_abi_version() == 3
+    assert L.nm_abi_version() == 4
 
 
 def test_status_strings(nm):

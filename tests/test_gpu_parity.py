@@ -9,6 +9,8 @@ Tolerances (the fp32 and bf16 bounds of the decode SpMV):
 Inputs for the CUDA path come from synth (seeded) or from the oracle; no
 oracle input comes from the CUDA path.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -323,6 +325,61 @@ def test_select_ties_and_special_values(nm):
         np.testing.assert_array_equal(to_bits(gv), ov)
 
 
+# --- selection and pack fused in one pass (nm_select_pack) ----------------------------
+
+@pytest.mark.parametrize("rows,K", PACK_SHAPES)
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_select_pack_bit_exact(nm, rows, K, N, M):
+    W = synth.weights(rows, K, seed=rows + K)
+    a = synth.col_norms(K, seed=rows + K)
+    om, ov = oracle.pack(oracle.select(to_bits(W), a.numpy(), N, M), N, M)
+    gm, gv = nm.select_pack(W.cuda(), a.cuda(), N, M)
+    np.testing.assert_array_equal(masks_np(gm), om)
+    np.testing.assert_array_equal(to_bits(gv), ov)
+
+
+def test_select_pack_ties_zeros_and_nan_scores(nm):
+    # weights +-1, 2, +0, -0 (ties, kept zeros with their sign), a column norm
+    # of 0 (a nonzero weight whose score ties the zeros), NaN weights and a NaN
+    # norm (NaN scores rank above every number)
+    rows, K = 96, 512
+    rng = np.random.default_rng(4)
+    W = np.array([0x3F80, 0xBF80, 0x4000, 0x0000, 0x8000], dtype=np.uint16)[rng.integers(0, 5, (rows, K))]
+    W[rng.integers(0, rows, 40), rng.integers(0, K, 40)] = 0x7FC0
+    a = np.ones(K, dtype=np.float32)
+    a[::7] = 0.0
+    a[5] = np.nan
+    for N, M in synth.PATTERNS:
+        om, ov = oracle.pack(oracle.select(W, a, N, M), N, M)
+        gm, gv = nm.select_pack(dev(W), torch.from_numpy(a).cuda(), N, M)
+        np.testing.assert_array_equal(masks_np(gm), om, err_msg=f"{N}:{M} masks")
+        np.testing.assert_array_equal(to_bits(gv), ov, err_msg=f"{N}:{M} values")
+
+
+@pytest.mark.parametrize("N,M", [(2, 4), (16, 32)])
+def test_select_pack_llama_gate_up_sampled(nm, N, M):
+    # full-size 28672 x 4096 on the GPU; rows sampled for the oracle
+    rows, K = synth.LLAMA31_8B["gate_up"]
+    W = synth.weights(rows, K, 0, 77, device="cuda")
+    a = synth.col_norms(K, 0, 78, device="cuda")
+    gm, gv = nm.select_pack(W, a, N, M)
+    idx = torch.from_numpy(np.random.default_rng(5).choice(rows, 64, replace=False)).cuda()
+    om, ov = oracle.pack(oracle.select(to_bits(W[idx].cpu()), a.cpu().numpy(), N, M), N, M)
+    np.testing.assert_array_equal(masks_np(gm[idx]), om)
+    np.testing.assert_array_equal(to_bits(gv[idx].cpu()), ov)
+
+
+def test_select_pack_rejects_bad_arguments(nm):
+    W = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    a = torch.ones(64, dtype=torch.float32, device="cuda")
+    with pytest.raises(nm.NmError) as e:
+        nm.select_pack(W, a, 1, 4)
+    assert e.value.status == nm.NM_ERR_UNSUPPORTED
+    with pytest.raises(nm.NmError) as e:
+        nm.select_pack(torch.zeros(4, 48, dtype=torch.bfloat16, device="cuda"), a[:48].contiguous(), 2, 4)
+    assert e.value.status == nm.NM_ERR_SHAPE
+
+
 def test_pack_fill_rule_and_signed_zero(nm):
     Wp = np.zeros((3, 64), dtype=np.uint16)
     Wp[0, 2] = 0x4000
@@ -551,6 +608,72 @@ def test_plan_falls_back_to_chained_launches(nm):
     for op, (m, v, x, _) in zip(ops, refs):
         assert torch.equal(op["y"], nm.spmv(m, v, x))
     plan.close()
+
+
+# --- q/k/v projection stored in three buffers (nm_spmv_qkv) ------------------------------------
+
+@pytest.mark.parametrize("batch", [1, 3, 8])
+@pytest.mark.parametrize("rows_q,rows_k,rows_v,K", [(4096, 1024, 1024, 4096), (96, 32, 32, 256),
+                                                    (100, 20, 30, 96), (0, 64, 64, 128), (64, 0, 40, 128)])
+def test_spmv_qkv(nm, rows_q, rows_k, rows_v, K, batch):
+    rows = rows_q + rows_k + rows_v
+    Wp = to_bits(synth.nm_structured(rows, K, 2, 4, seed=rows + K))
+    masks, values = oracle.pack(Wp, 2, 4)
+    xb = to_bits(synth.activations(batch, K, seed=batch + K))
+    y64, S = oracle.spmv_f64(Wp, xb)
+    m = torch.from_numpy(masks.view(np.int32)).cuda()
+    v, x = dev(values), dev(xb)
+    q, k, vv = nm.spmv_qkv(m, v, x, rows_q, rows_k)
+    y = nm.spmv(m, v, x)
+    torch.cuda.synchronize()
+    assert q.shape == (batch, rows_q) and k.shape == (batch, rows_k) and vv.shape == (batch, rows_v)
+    cat = torch.cat([q, k, vv], dim=1)
+    assert torch.equal(cat, y), "the three parts differ from nm_spmv's y"
+    check_bf16(to_bits(cat.cpu()), y64, S, f"qkv {rows_q}/{rows_k}/{rows_v} b{batch}")
+
+
+def test_qkv_op_in_a_plan_feeds_the_next_op(nm):
+    # qkv of a small layer stores q, k, v apart; the next op reads v as its x
+    rq, rk, rv, K = 256, 128, 128, 512
+    W1 = synth.nm_structured(rq + rk + rv, K, 4, 8, seed=41)
+    W2 = synth.nm_structured(96, rv, 4, 8, seed=42)
+    W2 = (W2.float() * (1.0 / (0.02 * (rv / 2) ** 0.5))).to(torch.bfloat16)
+    m1, v1 = nm.pack(W1.cuda(), 4, 8)
+    m2, v2 = nm.pack(W2.cuda(), 4, 8)
+    x = synth.activations(2, K, seed=43).cuda()
+    q = torch.full((2, rq), float("nan"), dtype=torch.bfloat16, device="cuda")
+    k = torch.full((2, rk), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vv = torch.full((2, rv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.full((2, 96), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ops = [dict(masks=m1, values=v1, x=x, y=q, y_k=k, y_v=vv, rows=rq + rk + rv, K=K, flags=nm.NM_LINEAR_QKV,
+                rows_q=rq, rows_k=rk),
+           dict(masks=m2, values=v2, x=vv, y=y2, rows=96, K=rv)]
+    for persistent in (False, True):  # persistent plans store plain y only: this one runs as a chain
+        plan = nm.StackPlan(ops, 2, persistent=persistent)
+        plan.run()
+        torch.cuda.synchronize()
+        full = nm.spmv(m1, v1, x)
+        assert torch.equal(torch.cat([q, k, vv], dim=1), full)
+        y64, S = oracle.spmv_f64(to_bits(W2), to_bits(vv.cpu()))
+        check_bf16(to_bits(y2.cpu()), y64, S, "op after qkv")
+        plan.close()
+    assert nm.device_status() == nm.NM_OK
+
+
+def test_spmv_qkv_rejects_bad_arguments(nm):
+    m = torch.zeros(64, 4, dtype=torch.int32, device="cuda")
+    v = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(1, 128, dtype=torch.bfloat16, device="cuda")
+    L = nm.lib()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    o = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda").data_ptr()
+    assert L.nm_spmv_qkv(m.data_ptr(), v.data_ptr(), x.data_ptr(), o, o, o, -1, 32, 32, 128, 1, s) == nm.NM_ERR_SHAPE
+    assert L.nm_spmv_qkv(m.data_ptr(), v.data_ptr(), x.data_ptr(), o, None, o, 32, 16, 16, 128, 1, s) == \
+        nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_qkv(m.data_ptr(), v.data_ptr(), x.data_ptr(), o + 2, o, o, 32, 16, 16, 128, 1, s) == \
+        nm.NM_ERR_ALIGN
+    assert L.nm_spmv_qkv(m.data_ptr(), v.data_ptr(), x.data_ptr(), o, o, o, 32, 16, 16, 128, 9, s) == \
+        nm.NM_ERR_UNSUPPORTED
 
 
 # --- gate/up SpMV with the SwiGLU epilogue ---------------------------------------------------
