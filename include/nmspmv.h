@@ -60,7 +60,9 @@ typedef enum nm_status {
     NM_ERR_NOT_NM = 5,      /* an M-subgroup holds more than N nonzeros */
     NM_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
     NM_ERR_TIMEOUT = 7,     /* a kernel's bounded wait ran out */
-    NM_ERR_NOT_PD = 8       /* nm_obs_prune: the damped Hessian is not positive definite */
+    NM_ERR_NOT_PD = 8,      /* nm_obs_prune: the damped Hessian is not positive definite */
+    NM_ERR_BOUNDS = 9       /* reported only by the bounds-checking build (NM_BOUNDS_CHECK): a
+                               kernel found an index outside its buffer and skipped the access */
 } nm_status;
 
 /* Version of this ABI (bumped on any incompatible change). */
@@ -340,7 +342,9 @@ nm_status nm_spmv_noalloc(const uint32_t *masks, const void *values_bf16, const 
 /*
  * nm_device_status -- waits for `stream`, then returns and clears the status
  * words of the current device: NM_ERR_TIMEOUT if any kernel's bounded wait ran
- * out since the last call, NM_OK otherwise (NM_ERR_CUDA if CUDA failed). It
+ * out since the last call, NM_ERR_BOUNDS if (in the bounds-checking build) a
+ * kernel skipped an access outside its buffer, NM_OK otherwise (NM_ERR_CUDA if
+ * CUDA failed). It
  * covers the library scratch and, once nm_spmv_noalloc has run on the device,
  * that call's static array. After a timeout it also clears the stream-K
  * counters (outputs of the calls that ran meanwhile are unspecified); call it

@@ -16,7 +16,8 @@ from typing import Iterable, Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libnmspmv.so")
+# NM_LIBRARY may name another build of the library (the bounds-checking one).
+LIB_PATH = os.environ.get("NM_LIBRARY") or os.path.join(_HERE, "libnmspmv.so")
 
 NM_OK = 0
 NM_ERR_INVALID_ARG = 1
@@ -27,6 +28,7 @@ NM_ERR_NOT_NM = 5
 NM_ERR_CUDA = 6
 NM_ERR_TIMEOUT = 7
 NM_ERR_NOT_PD = 8
+NM_ERR_BOUNDS = 9
 
 PATTERNS = ((2, 4), (4, 8), (8, 16), (16, 32))
 

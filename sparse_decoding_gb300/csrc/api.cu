@@ -4,10 +4,21 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 #include "streamk.cuh"
 
 namespace nm {
+
+// An NVTX range over one C entry point (visible in a timeline profiler; a
+// no-op when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr int kMaxDevices = 64;
 
@@ -318,6 +329,7 @@ const char *nm_status_str(int status)
     case NM_ERR_CUDA: return "CUDA error";
     case NM_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
     case NM_ERR_NOT_PD: return "the damped Hessian is not positive definite";
+    case NM_ERR_BOUNDS: return "a kernel skipped an access outside its buffer (bounds-checking build)";
     default: return "unknown status";
     }
 }
@@ -325,6 +337,7 @@ const char *nm_status_str(int status)
 nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M, void *W_pruned,
                     void *stream)
 {
+    NvtxRange nvtx_("nm_select");
     if (!pattern_ok(N, M))
         return NM_ERR_UNSUPPORTED;
     if (rows < 0 || K < 0 || (K % 32) != 0)
@@ -345,6 +358,7 @@ nm_status nm_select(const void *W_bf16, const float *a, int64_t rows, int64_t K,
 nm_status nm_select_pack(const void *W_bf16, const float *a, int64_t rows, int64_t K, int N, int M, uint32_t *masks,
                          void *values_bf16, void *stream)
 {
+    NvtxRange nvtx_("nm_select_pack");
     if (!pattern_ok(N, M))
         return NM_ERR_UNSUPPORTED;
     if (rows < 0 || K < 0 || (K % 32) != 0)
@@ -365,12 +379,14 @@ nm_status nm_select_pack(const void *W_bf16, const float *a, int64_t rows, int64
 nm_status nm_pack(const void *W_bf16, int64_t rows, int64_t K, int N, int M, uint32_t *masks, void *values_bf16,
                   void *stream)
 {
+    NvtxRange nvtx_("nm_pack");
     return pack_impl(W_bf16, nullptr, rows, K, N, M, masks, values_bf16, stream);
 }
 
 nm_status nm_pack_swiglu(const void *W_gate_bf16, const void *W_up_bf16, int64_t rows_h, int64_t K, int N, int M,
                          uint32_t *masks, void *values_bf16, void *stream)
 {
+    NvtxRange nvtx_("nm_pack_swiglu");
     if (rows_h % 16 != 0)
         return NM_ERR_SHAPE;
     if (rows_h > 0 && K > 0 && !W_up_bf16)
@@ -381,6 +397,7 @@ nm_status nm_pack_swiglu(const void *W_gate_bf16, const void *W_up_bf16, int64_t
 nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *h_bf16,
                          int64_t rows_h, int64_t K, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv_swiglu");
     if (rows_h < 0 || rows_h % 16 != 0)
         return NM_ERR_SHAPE;
     return spmv_impl(masks, values_bf16, x_bf16, h_bf16, kOutSwiglu, 2 * rows_h, K, batch, (cudaStream_t)stream,
@@ -390,18 +407,21 @@ nm_status nm_spmv_swiglu(const uint32_t *masks, const void *values_bf16, const v
 nm_status nm_spmv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *y_bf16, int64_t rows,
                   int64_t K, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv");
     return spmv_impl(masks, values_bf16, x_bf16, y_bf16, kOutBf16, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status nm_spmv_f32out(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
                          int64_t rows, int64_t K, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv_f32out");
     return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status nm_spmv_qkv(const uint32_t *masks, const void *values_bf16, const void *x_bf16, void *q_bf16, void *k_bf16,
                       void *v_bf16, int64_t rows_q, int64_t rows_k, int64_t rows_v, int64_t K, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv_qkv");
     nm_status s = check_qkv_parts(q_bf16, k_bf16, v_bf16, rows_q, rows_k, rows_v);
     if (s != NM_OK)
         return s;
@@ -417,23 +437,27 @@ nm_status nm_spmv_qkv(const uint32_t *masks, const void *values_bf16, const void
 nm_status nm_spmv_f32out_atomic(const uint32_t *masks, const void *values_bf16, const void *x_bf16, float *y_f32,
                                 int64_t rows, int64_t K, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv_f32out_atomic");
     return spmv_impl(masks, values_bf16, x_bf16, y_f32, kOutF32, rows, K, batch, (cudaStream_t)stream, false, true);
 }
 
 nm_status dense_gemv(const void *W_bf16, const void *x_bf16, void *y_bf16, int64_t rows, int64_t K, int batch,
                      void *stream)
 {
+    NvtxRange nvtx_("dense_gemv");
     return gemv_impl(W_bf16, x_bf16, y_bf16, false, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status dense_gemv_f32out(const void *W_bf16, const void *x_bf16, float *y_f32, int64_t rows, int64_t K,
                             int batch, void *stream)
 {
+    NvtxRange nvtx_("dense_gemv_f32out");
     return gemv_impl(W_bf16, x_bf16, y_f32, true, rows, K, batch, (cudaStream_t)stream, false);
 }
 
 nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream)
 {
+    NvtxRange nvtx_("nm_spmv_stack");
     if (n_ops < 0 || (n_ops > 0 && !ops))
         return NM_ERR_INVALID_ARG;
     for (int i = 0; i < n_ops; ++i) {
@@ -459,6 +483,7 @@ nm_status nm_spmv_stack(const nm_linear *ops, int n_ops, int batch, void *stream
 
 nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *stream)
 {
+    NvtxRange nvtx_("dense_gemv_stack");
     if (n_ops < 0 || (n_ops > 0 && !ops))
         return NM_ERR_INVALID_ARG;
     for (int i = 0; i < n_ops; ++i) {
@@ -477,6 +502,7 @@ nm_status dense_gemv_stack(const nm_linear *ops, int n_ops, int batch, void *str
 
 nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsigned flags, nm_stack_plan **plan)
 {
+    NvtxRange nvtx_("nm_stack_plan_create");
     if (!plan || n_ops < 0 || (n_ops > 0 && !ops) || (flags & ~(NM_STACK_DENSE | NM_STACK_PERSISTENT)))
         return NM_ERR_INVALID_ARG;
     const bool dense = (flags & NM_STACK_DENSE) != 0;
@@ -541,6 +567,7 @@ nm_status nm_stack_plan_create(const nm_linear *ops, int n_ops, int batch, unsig
 
 nm_status nm_stack_plan_run(const nm_stack_plan *plan, void *stream)
 {
+    NvtxRange nvtx_("nm_stack_plan_run");
     if (!plan)
         return NM_ERR_INVALID_ARG;
     int dev = -1;
@@ -570,6 +597,7 @@ nm_status nm_stack_plan_run(const nm_stack_plan *plan, void *stream)
 
 nm_status nm_stack_plan_destroy(nm_stack_plan *plan)
 {
+    NvtxRange nvtx_("nm_stack_plan_destroy");
     if (!plan)
         return NM_OK;
     nm_status s = NM_OK;
@@ -604,7 +632,7 @@ static nm_status read_clear_status(const Scratch &sc, size_t counter_bytes, cuda
         cudaMemsetAsync(sc.status, 0, sizeof word, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
     if (!(word & (1u << NM_ERR_TIMEOUT)))
-        return NM_OK;
+        return (word & (1u << NM_ERR_BOUNDS)) ? NM_ERR_BOUNDS : NM_OK;
     if (cudaMemsetAsync(sc.counters, 0, counter_bytes, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
     return NM_ERR_TIMEOUT;
@@ -612,6 +640,7 @@ static nm_status read_clear_status(const Scratch &sc, size_t counter_bytes, cuda
 
 nm_status nm_device_status(void *stream)
 {
+    NvtxRange nvtx_("nm_device_status");
     cudaStream_t st = (cudaStream_t)stream;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)

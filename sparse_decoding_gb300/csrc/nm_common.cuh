@@ -46,6 +46,27 @@ inline Scratch scratch_from_base(void *base)
 }
 
 // ---------------------------------------------------------------------------
+// Bounds-checking build
+// ---------------------------------------------------------------------------
+
+// With -DNM_BOUNDS_CHECK, NM_IN_BOUNDS(status, cond) checks an index that
+// depends on data or on the work split against its buffer: when cond fails it
+// sets the NM_ERR_BOUNDS bit of the status word and yields false, and the
+// caller skips the access. No trap, no assert. In the normal build it is the
+// constant true and compiles away.
+__device__ __forceinline__ bool bounds_ok(uint32_t *status, bool cond)
+{
+    if (!cond)
+        atomicOr(status, 1u << NM_ERR_BOUNDS);
+    return cond;
+}
+#ifdef NM_BOUNDS_CHECK
+#define NM_IN_BOUNDS(status, cond) ::nm::bounds_ok((status), (cond))
+#else
+#define NM_IN_BOUNDS(status, cond) true
+#endif
+
+// ---------------------------------------------------------------------------
 // bf16 bits
 // ---------------------------------------------------------------------------
 

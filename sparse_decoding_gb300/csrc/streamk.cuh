@@ -202,6 +202,8 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
     const int64_t first = div64(((rb_lo + 1) * (P)) - 1, U);
     const int64_t last = div64(((rb_hi) * (P)) - 1, U);
     const int slot = (rb == div64(cr.cs, KC)) ? 0 : 1;
+    if (!NM_IN_BOUNDS(p.scratch.status, c < kMaxCtas && first <= last && last < P && first >= 0))
+        return;
     float *mine = p.scratch.partials + (c * 2 + slot) * (8 * 32) + lane;
 #pragma unroll
     for (int b = 0; b < B; ++b)
@@ -226,7 +228,7 @@ __device__ __forceinline__ void finish_across_ctas(const StreamKParams &p, const
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t cc = c0 + j;
-            if (cc <= last) {
+            if (cc <= last && NM_IN_BOUNDS(p.scratch.status, cc < kMaxCtas)) {
                 const int cslot = (rb == div64(muldiv(U, cc, P), KC)) ? 0 : 1;
                 const float *q = p.scratch.partials + (cc * 2 + cslot) * (8 * 32) + lane;
 #pragma unroll
@@ -284,10 +286,11 @@ __device__ __forceinline__ void finish_in_cta(const StreamKParams &p, const CtaR
         for (int j = 0; j < 4; ++j) {
             const int w = w0 + j;
             const int ws = w == first ? slot_first : 0;
+            const bool in = w <= last && NM_IN_BOUNDS(p.scratch.status, w >= 0 && w < cr.nw);
             const float *q = part + ((w * 2 + ws) * B) * 32 + lane;
 #pragma unroll
             for (int b = 0; b < B; ++b)
-                v[j][b] = w <= last ? q[b * 32] : 0.f;
+                v[j][b] = in ? q[b * 32] : 0.f;
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -469,7 +472,7 @@ __device__ __forceinline__ void consume_range(const TensorMaps *maps, const Stre
         typename Pol::template Regs<B> r;
         Pol::template load<B>(stage0p + s * SB, lane, r);
         __syncwarp(); // every lane's reads of the stage are done
-        if (i + NBUF < n) {
+        if (i + NBUF < n && NM_IN_BOUNDS(p.scratch.status, pkc < KC && (int64_t)prb * kUnitRows < p.rows)) {
             if (lane == 0 && !dead) {
                 const uint32_t jn = j + NBUF;
                 fence_proxy_async_smem();
@@ -494,7 +497,7 @@ __device__ __forceinline__ void consume_range(const TensorMaps *maps, const Stre
             }
             if (seg_kc0 == 0 && kc + 1 == KC) {
                 store_y<B, OUT>(p, (int64_t)rb * kUnitRows + lane, tot); // a whole row block
-            } else {
+            } else if (NM_IN_BOUNDS(p.scratch.status, warp < W && (rb == w.rb0 || rb == (int32_t)div64(w.ue - 1, KC)))) {
                 float *mine = part + ((warp * 2 + (rb == w.rb0 ? 0 : 1)) * B) * 32 + lane;
 #pragma unroll
                 for (int b = 0; b < B; ++b)
@@ -639,7 +642,7 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
         uint32_t un = 0xFFFFFFFFu;
         if (lane == 0 && !dead) {
             un = atomicAdd(qv.claim, 1u);
-            if (un < n) {
+            if (un < n && NM_IN_BOUNDS(p.scratch.status, un < (uint32_t)queue_cap<W>())) {
                 int32_t rb, kc;
                 queue_unit_coords(p, qb, un, rb, kc);
                 qv.stage_unit[warp * NBUF + s] = un;
@@ -661,7 +664,7 @@ __device__ __forceinline__ void consume_queue(const TensorMaps *maps, const Stre
             for (int b = 0; b < B; ++b)
                 acc[q][b] = 0.f;
         Pol::template compute<B>(r, xringp + xs * XB, xfp, pol_smem, pst, lane, acc);
-        if (u < n)
+        if (u < n && NM_IN_BOUNDS(p.scratch.status, u < (uint32_t)queue_cap<W>() && xs <= (uint32_t)NBUF))
             qv.upart[u * 32 + lane] = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
         xs = xs == NBUF ? 0 : xs + 1;
     }

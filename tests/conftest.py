@@ -17,3 +17,15 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _status_clean_in_checking_build(request):
+    """With NM_LIBRARY naming another build (the bounds-checking one), every GPU
+    test must leave the device status word clean: no index out of its buffer,
+    no bounded wait run out."""
+    yield
+    if os.environ.get("NM_LIBRARY") and request.node.get_closest_marker("gpu"):
+        import sparse_decoding_gb300 as nm
+        st = nm.device_status()
+        assert st == nm.NM_OK, f"device status after the test: {nm.status_str(st)}"

@@ -61,9 +61,9 @@ def test_library_exports_every_declared_symbol(nm):
 
 
 def test_status_strings(nm):
-    for code in range(9):
+    for code in range(10):
         assert nm.status_str(code) != "unknown status"
-    assert nm.status_str(9) == "unknown status"
+    assert nm.status_str(10) == "unknown status"
     assert nm.status_str(5).startswith("an M-subgroup")
 
 

@@ -208,6 +208,17 @@ def test_spmv_70b_batch_sweep_sampled(nm, batch, name):
     check_sampled(nm, rows, K, 2, 4, batch, seed=31 + batch, what=f"70b {name} b{batch}")
 
 
+# The 8B stack's two largest linears at full size at the batch sizes of the
+# batch-4 and batch-8 timings (the batch > 1 kernel: bf16 x window, per-warp
+# ranges, fix-ups between warps and CTAs), all four patterns.
+@pytest.mark.parametrize("batch", [4, 8])
+@pytest.mark.parametrize("name", ["gate_up", "down"])
+@pytest.mark.parametrize("N,M", synth.PATTERNS)
+def test_spmv_llama8b_batch_sampled(nm, batch, name, N, M):
+    rows, K = synth.LLAMA31_8B[name]
+    check_sampled(nm, rows, K, N, M, batch, seed=61 + batch + N, what=f"8b {name} {N}:{M} b{batch}")
+
+
 @pytest.mark.parametrize("N,M", synth.PATTERNS)
 def test_spmv_exact_dyadic(nm, N, M):
     """Dyadic weights, small-integer x: fp32 is exact in any summation order."""
