@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "libnmspmv.so")
 BUILD_CHECK = os.path.join(HERE, "_build_check")
 LIB_CHECK = os.path.join(HERE, "libnmspmv_check.so")
 
-SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "noalloc.cu", "obs.cu", "pack_host.cpp"]
+SOURCES = ["api.cu", "spmv.cu", "gemv.cu", "pack.cu", "noalloc.cu", "obs.cu", "tc_gemm.cu", "pack_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -51,13 +51,6 @@ def _compile(src: str, check: bool = False) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def _rpath():
-    """Run-time search path for cuBLAS: the toolkit that nvcc belongs to."""
-    root = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
-    dirs = [d for d in (os.path.join(root, "lib64"), os.path.join(root, "lib")) if os.path.isdir(d)]
-    return [f"-Xlinker=-rpath={d}" for d in dirs]
-
-
 def _stale(lib: str = LIB) -> bool:
     if not os.path.exists(lib):
         return True
@@ -83,7 +76,7 @@ def build(force: bool = False, verbose: bool = False, check: bool = False) -> st
             f.write(f"==== {src}\n{log}\n")
     tmp = lib + f".tmp{os.getpid()}"
     cmd = ([nvcc(), "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC"]
-           + ["-lcublas", "-ldl"] + _rpath())
+           + ["-ldl"])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

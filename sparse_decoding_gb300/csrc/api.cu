@@ -63,6 +63,15 @@ static nm_status device_ctx(cudaStream_t stream, bool pdl, LaunchCtx *ctx)
     return NM_OK;
 }
 
+nm_status library_status_word(uint32_t **status)
+{
+    LaunchCtx ctx;
+    nm_status s = device_ctx(nullptr, false, &ctx);
+    if (s == NM_OK)
+        *status = ctx.scratch.status;
+    return s;
+}
+
 EncodeTiledFn encode_tiled_fn()
 {
     static std::once_flag once;

@@ -67,6 +67,31 @@ nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t
 nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
                              const LaunchCtx &ctx);
 
+// ---- tensor-core GEMM of the OBS pruning (tc_gemm.cu) ----
+// C = alpha A B^T + beta C: A bf16 [M][kp], B bf16 [N][kp] (kp a multiple of
+// 64, rows contiguous along k), C fp32 with row stride ldc (16-byte aligned,
+// N and ldc multiples of 4). With nparts > 1 the k-tiles cycle through part
+// slots; slot 0 accumulates apart from the others. A bounded wait that runs
+// out sets NM_ERR_TIMEOUT in *status.
+nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kp, int nparts, float *C, int64_t ldc, int64_t M,
+                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st);
+// fp32 C = alpha A op(B) + beta C with fp32 emulated by bf16 parts (six
+// products): A (M x k) row-major with stride lda (a_trans: stored k x M);
+// op(B) = B^T for B (N x k) row-major, or B for B (k x N) row-major when
+// b_trans. work_a / work_b: tc_operand_bytes(M or N, k, true) bytes each
+// (the k range is done in chunks of 1024, whose results add up in C).
+nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B, int64_t ldb, bool b_trans, int64_t M,
+                      int64_t N, int64_t k, float *C, int64_t ldc, float alpha, float beta, uint16_t *work_a,
+                      uint16_t *work_b, uint32_t *status, cudaStream_t st);
+size_t tc_operand_bytes(int64_t rows, int64_t k, bool emulated);
+// Xt [K][Tp] = X^T (bf16 X [T][K]), zero in columns T .. Tp.
+nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *Xt, int64_t Tp, cudaStream_t st);
+// The same product in plain fp32 on the CUDA cores (b_kn: B stored k x N).
+nm_status simt_gemm_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
+                        int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st);
+// The library scratch's status word on the current device (allocated if need be).
+nm_status library_status_word(uint32_t **status);
+
 // The static scratch of nm_spmv_noalloc on device `dev`, if a call has set it
 // up there (noalloc.cu).
 bool noalloc_scratch(int dev, Scratch *out);

@@ -36,15 +36,17 @@
 //   5. the lazy update P += D R, in two levels: the rest of the current
 //      1024-column superblock after each block, every later column once per
 //      superblock (one GEMM with k up to 1024).
-// Every GEMM is cuBLAS fp32: by default emulated on the bf16 tensor cores
-// (each operand split into 3 bf16 terms), with NM_OBS_SGEMM plain fp32.
-#include <cublas_v2.h>
+// Every GEMM runs on this library's tensor-core GEMM (tc_gemm.cu): fp32
+// emulated by three bf16 parts per operand and the six products of order up
+// to 2, accumulated in fp32 in tensor memory; with NM_OBS_SGEMM, plain fp32 on
+// the CUDA cores instead. The Hessian is one bf16 pass (its products are exact).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
-#include "nmspmv.h"
+#include "kernels.h"
 
 namespace nm {
 namespace {
@@ -53,7 +55,6 @@ constexpr int kObsBlock = 128;   // columns per sweep block
 constexpr int kSuper = 1024;     // columns per lazy-update superblock (a multiple of kObsBlock)
 constexpr int kSweepWarps = 16;  // rows in flight per CTA
 constexpr int kMaxDevices = 64;
-const float kOne = 1.0f;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -506,11 +507,10 @@ cudaError_t sweep(int M, const SweepArgs &a, int i1, int bw, int grid, cudaStrea
 // ---- host side ----------------------------------------------------------------
 
 struct ObsDevice {
-    cublasHandle_t blas = nullptr;
     int sms = 0;
 };
 
-std::mutex g_obs_mu;  // held for the whole of each call (the handle is shared)
+std::mutex g_obs_mu;  // held for the whole of each call
 ObsDevice g_obs[kMaxDevices];
 
 nm_status obs_device(ObsDevice **out)
@@ -521,16 +521,6 @@ nm_status obs_device(ObsDevice **out)
     ObsDevice &d = g_obs[dev];
     if (!d.sms && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return NM_ERR_CUDA;
-    if (!d.blas) {
-        // the inputs are finite, so the emulated GEMMs need no pass for infinities or NaN
-        if (cublasCreate(&d.blas) != CUBLAS_STATUS_SUCCESS) {
-            d.blas = nullptr;
-            return NM_ERR_CUDA;
-        }
-        if (cublasSetEmulationSpecialValuesSupport(d.blas, CUDA_EMULATION_SPECIAL_VALUES_SUPPORT_NONE) !=
-            CUBLAS_STATUS_SUCCESS)
-            return NM_ERR_CUDA;
-    }
     *out = &d;
     return NM_OK;
 }
@@ -565,25 +555,33 @@ struct Workspace {
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Row-major fp32 GEMMs on K-strided buffers, through cuBLAS's column-major
-// interface (a row-major p x q block is the column-major q x p transpose).
+// Row-major fp32 GEMMs on K-strided buffers: on the tensor cores with fp32
+// emulated by bf16 parts (wa, wb: the split operands' workspace), or plain
+// fp32 on the CUDA cores.
 struct RowGemm {
-    cublasHandle_t h;
-    cublasComputeType_t ct;
-    int ld;
+    bool plain;
+    int64_t ld;
+    uint16_t *wa, *wb;
+    uint32_t *status;
+    cudaStream_t st;
+    // C (M x N) = alpha * A (M x k, stride lda) * op(B) + beta * C (stride ldc);
+    // op(B) = B (k x N) when b_kn, else B^T (B is N x k)
+    bool gemm(int64_t M, int64_t N, int64_t k, float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+              bool b_kn, float beta, float *C, int64_t ldc) const
+    {
+        if (plain)
+            return simt_gemm_f32(A, lda, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, st) == NM_OK;
+        return tc_gemm_f32(A, lda, false, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, wa, wb, status, st) == NM_OK;
+    }
     // C (r x c) = alpha * A (r x k) * B (k x c) + beta * C
     bool ab(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
     {
-        return cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, (int)c, (int)r, (int)k, &alpha, B, CUDA_R_32F, ld, A,
-                            CUDA_R_32F, ld, &beta, C, CUDA_R_32F, ld, ct, CUBLAS_GEMM_DEFAULT) ==
-               CUBLAS_STATUS_SUCCESS;
+        return gemm(r, c, k, alpha, A, ld, B, ld, true, beta, C, ld);
     }
     // C (r x c) = alpha * A (r x k) * B^T (B is c x k) + beta * C
     bool abt(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
     {
-        return cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)c, (int)r, (int)k, &alpha, B, CUDA_R_32F, ld, A,
-                            CUDA_R_32F, ld, &beta, C, CUDA_R_32F, ld, ct, CUBLAS_GEMM_DEFAULT) ==
-               CUBLAS_STATUS_SUCCESS;
+        return gemm(r, c, k, alpha, A, ld, B, ld, false, beta, C, ld);
     }
 };
 
@@ -644,18 +642,23 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     nm_status s = obs_device(&d);
     if (s != NM_OK)
         return s;
-    if (cublasSetStream(d->blas, st) != CUBLAS_STATUS_SUCCESS)
-        return NM_ERR_CUDA;
     const bool plain = (flags & NM_OBS_SGEMM) != 0;
-    const RowGemm G{d->blas, plain ? CUBLAS_COMPUTE_32F : CUBLAS_COMPUTE_32F_EMULATED_16BFX9, (int)K};
+    const int64_t nb = (K + kFacB - 1) / kFacB;
 
-    // buffers: dead flags, lam, the not-PD flag, three K x K matrices (A, later
-    // R; L; X), D of one superblock, the accumulator P
+    // buffers: dead flags, lam, the not-PD flag and the GEMMs' status word,
+    // three K x K matrices (A, later R; L; X), D of one superblock, the
+    // accumulator P, and the bf16 parts of the two operands of one GEMM (none
+    // for plain fp32). The recursion's operands are at most Kh x Kh; the lazy
+    // update's are D (rows x superblock) and a part of R (K x superblock).
+    const int64_t Kh = ((nb + 1) / 2) * kFacB < K ? ((nb + 1) / 2) * kFacB : K;
+    const size_t wa_bytes = plain ? 0 : std::max(tc_operand_bytes(Kh, Kh, true), tc_operand_bytes(rows, kSuper, true));
+    const size_t wb_bytes = plain ? 0 : std::max(tc_operand_bytes(Kh, Kh, true), tc_operand_bytes(K, kSuper, true));
     const size_t kk = (size_t)K * K * 4;
     const size_t off_lam = round256((size_t)K), off_flag = off_lam + 256, off_A = off_flag + 256;
     const size_t off_L = off_A + round256(kk), off_X = off_L + round256(kk), off_D = off_X + round256(kk);
     const size_t off_P = off_D + round256((size_t)rows * kSuper * 4);
-    const size_t total = off_P + round256((size_t)rows * K * 4);
+    const size_t off_WA = off_P + round256((size_t)rows * K * 4), off_WB = off_WA + round256(wa_bytes);
+    const size_t total = off_WB + round256(wb_bytes);
     Workspace ws(st);
     if (!ws.alloc(total))
         return NM_ERR_CUDA;
@@ -663,18 +666,19 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     unsigned char *dead = (unsigned char *)base;
     float *lam = (float *)(base + off_lam);
     int *not_pd = (int *)(base + off_flag);
+    uint32_t *gemm_status = (uint32_t *)(base + off_flag + 16);
     float *A = (float *)(base + off_A), *L = (float *)(base + off_L), *X = (float *)(base + off_X);
     float *Dbuf = (float *)(base + off_D), *P = (float *)(base + off_P);
     float *R = A;  // R replaces A once the factorisation is done
+    const RowGemm G{plain, K, (uint16_t *)(base + off_WA), (uint16_t *)(base + off_WB), gemm_status, st};
 
-    if (cudaMemsetAsync(not_pd, 0, sizeof(int), st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess ||
+    if (cudaMemsetAsync(base + off_flag, 0, 256, st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess ||
         cudaMemsetAsync(P, 0, (size_t)rows * K * 4, st) != cudaSuccess)
         return NM_ERR_CUDA;
     obs_diag_kernel<<<1, 1024, 0, st>>>(H, K, percdamp, dead, lam);
     obs_reverse_damp_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(H, K, lam, A);
     if (cudaGetLastError() != cudaSuccess)
         return NM_ERR_CUDA;
-    const int64_t nb = (K + kFacB - 1) / kFacB;
     if (!chol_inv(G, A, L, X, K, 0, nb, false, not_pd, st))
         return NM_ERR_CUDA;
     // A pivot that is not positive was replaced by 1, so the rest runs on
@@ -696,9 +700,7 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
                        Wout_f32, masks};
     auto update = [&](int64_t c0, int64_t c1, int64_t k0, int64_t kw, const float *Dk) {
         // P[:, c0:c1] += D[:, k0 ...] R[k0:k0+kw, c0:c1]   (D rows have stride kSuper)
-        return cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_N, (int)(c1 - c0), (int)rows, (int)kw, &kOne,
-                            R + k0 * K + c0, CUDA_R_32F, (int)K, Dk, CUDA_R_32F, kSuper, &kOne, P + c0, CUDA_R_32F,
-                            (int)K, G.ct, CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+        return G.gemm(rows, c1 - c0, kw, 1.0f, Dk, kSuper, R + k0 * K + c0, K, true, 1.0f, P + c0, K);
     };
     constexpr int64_t kPerSuper = kSuper / kObsBlock;
     for (int64_t sb = 0; sb < nb; sb += kPerSuper) {
@@ -715,12 +717,14 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
         if (s2 < K && !update(s2, K, s1, s2 - s1, Dbuf))
             return NM_ERR_CUDA;
     }
-    int host_flag = 0;
+    int host_flag[5] = {0, 0, 0, 0, 0}; // not-PD flag, then (16 bytes on) the GEMMs' status word
     if (cudaGetLastError() != cudaSuccess ||
-        cudaMemcpyAsync(&host_flag, not_pd, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(host_flag, not_pd, sizeof host_flag, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return NM_ERR_CUDA;
-    return host_flag ? NM_ERR_NOT_PD : NM_OK;
+    if (host_flag[4] & (1 << NM_ERR_TIMEOUT))
+        return NM_ERR_TIMEOUT;
+    return host_flag[0] ? NM_ERR_NOT_PD : NM_OK;
 }
 
 }  // namespace
@@ -743,19 +747,22 @@ extern "C" nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, fl
         return accumulate ? NM_OK
                           : (cudaMemsetAsync(H, 0, (size_t)K * K * 4, st) == cudaSuccess ? NM_OK : NM_ERR_CUDA);
     std::lock_guard<std::mutex> lock(g_obs_mu);
-    ObsDevice *d = nullptr;
-    nm_status s = obs_device(&d);
+    // H[i][j] = 2 sum_t X[t][i] X[t][j]: X^T (bf16 [K][Tp], t contiguous, zero
+    // padding to a multiple of 64 tokens) is both operands of one bf16 pass;
+    // the products are exact and the sums fp32. A bounded wait that runs out
+    // is reported by nm_device_status.
+    uint32_t *status = nullptr;
+    nm_status s = library_status_word(&status);
     if (s != NM_OK)
         return s;
-    if (cublasSetStream(d->blas, st) != CUBLAS_STATUS_SUCCESS)
+    const int64_t Tp = (T + 63) / 64 * 64;
+    Workspace ws(st);
+    if (!ws.alloc((size_t)K * Tp * 2))
         return NM_ERR_CUDA;
-    // column-major view: X is K x T (ld K); H = 2 X X^T is K x K
-    const float alpha = 2.0f, beta = accumulate ? 1.0f : 0.0f;
-    if (cublasGemmEx(d->blas, CUBLAS_OP_N, CUBLAS_OP_T, (int)K, (int)K, (int)T, &alpha, X_bf16, CUDA_R_16BF, (int)K,
-                     X_bf16, CUDA_R_16BF, (int)K, &beta, H, CUDA_R_32F, (int)K, CUBLAS_COMPUTE_32F,
-                     CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
-        return NM_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    uint16_t *Xt = (uint16_t *)ws.p;
+    if ((s = tc_transpose_bf16((const uint16_t *)X_bf16, T, K, Xt, Tp, st)) != NM_OK)
+        return s;
+    return tc_gemm_bf16(Xt, Xt, Tp, 1, H, K, K, K, 2.0f, accumulate ? 1.0f : 0.0f, status, st);
 }
 
 extern "C" nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t rows, int64_t K, int N, int M,

@@ -1,0 +1,552 @@
+// tc_gemm.cu -- the GEMM-shaped steps of the OBS pruning on the 5th-generation
+// tensor cores (tcgen05), with the operands staged by TMA and the accumulator
+// in tensor memory.
+//
+//   C = alpha * A * B^T + beta * C     A: bf16 [M][k], B: bf16 [N][k] (rows
+//                                      contiguous along k), C: fp32 [M][N]
+//
+// One CTA computes a 128 x 128 tile of C: warp 0 (one thread) streams 64-wide
+// k-tiles of A and B into a ring of shared-memory stages by TMA (128-byte
+// swizzle); warp 1 (one thread) issues four M=128, N=128, K=16 tcgen05.mma per
+// stage into 128-column fp32 accumulators in tensor memory (four of them, see
+// below) and releases the stage with tcgen05.commit; at the end all four warps
+// read the accumulators with tcgen05.ld (warp w: rows 32w..32w+31, one row per
+// thread), add them, and write C.
+//
+// fp32 products (the Cholesky steps and the lazy update) are emulated with
+// bf16 parts: a = a0 + a1 + a2 with a0 = bf16(a), a1 = bf16(a - a0),
+// a2 = bf16(a - a0 - a1) (together 24 bits of a's significand), and
+//   a b ~ a0 b0 + a0 b1 + a1 b0 + a0 b2 + a1 b1 + a2 b0
+// -- every product of order up to 2 -- accumulated in fp32; the dropped terms
+// are below 2^-24 |a b|. split_kernel writes the parts of a fp32 matrix as one
+// bf16 operand whose k dimension interleaves them per 64-column tile (A side:
+// a0 a0 a1 a0 a1 a2; B side: b0 b1 b0 b2 b1 b0), so that one bf16 GEMM over a
+// six times longer k forms exactly those six products. The leading products
+// a0 b0 of successive k-tiles take turns in three tensor-memory accumulators
+// and the five smaller ones go to a fourth; the four are added once at the
+// end, in a fixed order. The tensor cores' accumulation loses more than fp32
+// rounding as k grows (in one accumulator, the mean error at k = 2048 was 2.8
+// times that of fp32 on the CUDA cores); spreading k over several
+// accumulators keeps each sum shorter. The Hessian's operand (bf16
+// calibration inputs, transposed) needs one part: its products are exact, and
+// its k-tiles take turns in all four accumulators.
+//
+// Every wait is bounded (about a second); a wait that runs out sets a flag the
+// host reads, and the kernel still frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace nm {
+namespace {
+
+constexpr int kTcM = 128;        // rows of C per CTA (tensor-memory lanes)
+constexpr int kTcN = 128;        // columns of C per CTA (tensor-memory columns)
+constexpr int kTcK = 64;         // k per stage: one 128-byte swizzled row of bf16
+constexpr int kTcStages = 4;
+constexpr int kTcTileBytes = kTcM * kTcK * 2;              // 16 KB (A; B is the same)
+constexpr int kTcStageBytes = 2 * kTcTileBytes;            // A + B
+constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024;  // + alignment slack
+constexpr int kTcThreads = 128;
+
+// ---- tensor-memory and tensor-core instructions (PTX ISA, tcgen05) ----------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tensor memory) (+)= A (shared, descriptor) * B (shared, descriptor)^T
+__device__ __forceinline__ void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+// Arrive on an mbarrier once every tcgen05.mma issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                 "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (the
+// stride byte offset), start address in 16-byte units, descriptor version 1,
+// layout type 2 (128-byte swizzle). The leading byte offset is not used by
+// this layout. The tile starts on a 1024-byte boundary (base offset 0); a
+// k-slice of 16 elements inside it starts 32 bytes further per slice.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused): 16 bytes
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 1024 bytes
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major,
+// M = 128, N = 128.
+constexpr uint32_t kIdescBf16 = (1u << 4)               // D format: fp32
+                                | (1u << 7)             // A format: bf16
+                                | (1u << 10)            // B format: bf16
+                                | ((kTcN >> 3) << 17)   // N / 8
+                                | ((kTcM >> 4) << 24);  // M / 16
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, 1u << NM_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// The accumulator of k-tile t (a) and whether t is the first tile it gets.
+// One part (nparts == 1): tiles take turns in all four accumulators. Several
+// (fp32 emulated): tile t holds part slot t % nparts; slot 0, the leading
+// products, takes turns in accumulators 0..2 by part group t / nparts, and
+// the other slots all go to accumulator 3 (first used by tile 1).
+constexpr int kTcAcc = 4;
+__device__ __forceinline__ void tc_route(int t, int nparts, int &a, bool &first)
+{
+    if (nparts == 1) {
+        a = t % kTcAcc;
+        first = t < kTcAcc;
+        return;
+    }
+    const int slot = t % nparts, group = t / nparts;
+    if (slot == 0) {
+        a = group % (kTcAcc - 1);
+        first = group < kTcAcc - 1;
+    } else {
+        a = kTcAcc - 1;
+        first = t == 1;
+    }
+}
+
+struct TcMaps {
+    CUtensorMap a;  // bf16 [M][kp], box 64 x 128, 128-byte swizzle
+    CUtensorMap b;  // bf16 [N][kp], box 64 x 128, 128-byte swizzle
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, float *C, int64_t ldc, int M, int N, int ktiles, int nparts,
+                   float alpha, float beta, uint32_t *err)
+{
+    __shared__ __align__(8) uint64_t full_bar[kTcStages];
+    __shared__ __align__(8) uint64_t empty_bar[kTcStages];
+    __shared__ __align__(8) uint64_t done_bar;
+    __shared__ uint32_t tmem_base;
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+    uint8_t *const tiles = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
+    const uint32_t tiles0 = smem_addr(tiles);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kTcN, m0 = blockIdx.y * kTcM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1);
+            mbar_init(smem_addr(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_addr(&done_bar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 2)
+        tmem_alloc(smem_addr(&tmem_base), kTcAcc * kTcN); // four 128-column fp32 accumulators
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // producer: k-tile t goes to stage t % S, once the MMAs of tile t - S have released it
+        int issued = 0;
+        for (int t = 0; t < ktiles; ++t) {
+            const int s = t % kTcStages;
+            if (t >= kTcStages && !wait_bounded(smem_addr(&empty_bar[s]), ((t / kTcStages) - 1) & 1, err))
+                break;
+            const uint32_t fb = smem_addr(&full_bar[s]);
+            mbar_arrive_expect_tx(fb, kTcStageBytes);
+            const uint32_t sa = tiles0 + s * kTcStageBytes;
+            tma_load_2d(sa, &maps.a, t * kTcK, m0, fb);
+            tma_load_2d(sa + kTcTileBytes, &maps.b, t * kTcK, n0, fb);
+            issued = t + 1;
+        }
+        // before leaving, let the copies that may still be in flight land (bounded)
+        for (int t = issued - kTcStages > 0 ? issued - kTcStages : 0; t < issued; ++t)
+            if (!wait_bounded(smem_addr(&full_bar[t % kTcStages]), (t / kTcStages) & 1, err))
+                break;
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        bool ok = true;
+        for (int t = 0; t < ktiles && ok; ++t) {
+            const int s = t % kTcStages;
+            ok = wait_bounded(smem_addr(&full_bar[s]), (t / kTcStages) & 1, err);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t sa = tiles0 + s * kTcStageBytes;
+            int a;
+            bool first;
+            tc_route(t, nparts, a, first);
+            const uint32_t acc = tmem + (uint32_t)(a * kTcN);
+#pragma unroll
+            for (int k = 0; k < kTcK / 16; ++k) {
+                const uint64_t ad = smem_desc_sw128(sa + k * 32);
+                const uint64_t bd = smem_desc_sw128(sa + kTcTileBytes + k * 32);
+                tc_mma_bf16(acc, ad, bd, kIdescBf16, (first && k == 0) ? 0u : 1u);
+            }
+            tc_commit(smem_addr(&empty_bar[s])); // the stage is free once these MMAs are done
+        }
+        tc_commit(smem_addr(&done_bar)); // the accumulator is complete once every MMA is done
+    }
+    __syncwarp();
+    // epilogue: every warp waits for the accumulator, then reads its 32 lanes
+    const bool have = wait_bounded(smem_addr(&done_bar), 0, err) && ktiles > 0;
+    tc_fence_after();
+    const int row = m0 + warp * 32 + lane;
+    // the accumulators that received a k-tile, added in index order
+    uint32_t used = 0;
+    for (int t = 0; t < ktiles && t < 4 * nparts; ++t) {
+        int a;
+        bool first;
+        tc_route(t, nparts, a, first);
+        used |= 1u << a;
+    }
+#pragma unroll 1
+    for (int c = 0; c < kTcN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
+#pragma unroll 1
+        for (int a = 1; a < kTcAcc; ++a) {
+            if (!(used & (1u << a)))
+                continue;
+            uint32_t r2[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * kTcN + c), r2);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+        }
+        if (row >= M || n0 + c >= N)
+            continue;
+        float *dst = C + (int64_t)row * ldc + n0 + c;
+        const int ncol = N - (n0 + c) < 32 ? N - (n0 + c) : 32; // a multiple of 4
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            if (j < ncol) {
+                float4 v;
+                v.x = have ? alpha * __uint_as_float(r[j]) : 0.f;
+                v.y = have ? alpha * __uint_as_float(r[j + 1]) : 0.f;
+                v.z = have ? alpha * __uint_as_float(r[j + 2]) : 0.f;
+                v.w = have ? alpha * __uint_as_float(r[j + 3]) : 0.f;
+                if (beta != 0.f) {
+                    const float4 o = *(const float4 *)(dst + j);
+                    v.x = fmaf(beta, o.x, v.x);
+                    v.y = fmaf(beta, o.y, v.y);
+                    v.z = fmaf(beta, o.z, v.z);
+                    v.w = fmaf(beta, o.w, v.w);
+                }
+                *(float4 *)(dst + j) = v;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2)
+        tmem_dealloc(tmem, kTcAcc * kTcN);
+}
+
+// ---- operand preparation ------------------------------------------------------
+
+// The bf16 parts of a fp32 value: a0 = bf16(a), a1 = bf16(a - a0),
+// a2 = bf16(a - a0 - a1) (each difference exact in fp32).
+__device__ __forceinline__ void split3(float a, uint16_t &p0, uint16_t &p1, uint16_t &p2)
+{
+    p0 = f32_to_bf16_rn(a);
+    const float r1 = a - __uint_as_float((uint32_t)p0 << 16);
+    p1 = f32_to_bf16_rn(r1);
+    const float r2 = r1 - __uint_as_float((uint32_t)p1 << 16);
+    p2 = f32_to_bf16_rn(r2);
+}
+
+// Out [rows][kt * 6 * 64] bf16: for row r and k-tile t, six 64-wide slots of
+// parts of S's elements (r, 64 t .. 64 t + 63) in the order `order` (two bits
+// per slot: the part index), zero beyond k or rows. S is fp32 with row stride
+// lds, read as S[r][c] or, transposed, as S[c][r]. A CTA covers 32 rows x 32
+// columns through a shared tile (the transposed read stays coalesced).
+__global__ void __launch_bounds__(256)
+    split_kernel(const float *__restrict__ S, int64_t lds, int rows, int k, int trans, uint32_t order,
+                 uint16_t *__restrict__ out, int kt)
+{
+    __shared__ float tile[32][33];
+    const int64_t op = (int64_t)kt * 6 * kTcK; // out row pitch (elements)
+    // blocks cover 32 rows x 32 source columns
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5; // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        float v = 0.f;
+        if (!trans) {
+            const int r = r0 + i, c = c0 + tx;
+            if (r < rows && c < k)
+                v = S[(int64_t)r * lds + c];
+            tile[i][tx] = v;
+        } else {
+            // element (row r, column c) of the operand is S[c][r]: read S rows c0+i, columns r0+tx
+            const int c = c0 + i, r = r0 + tx;
+            if (r < rows && c < k)
+                v = S[(int64_t)c * lds + r];
+            tile[tx][i] = v;
+        }
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int r = r0 + i, c = c0 + tx;
+        if (r >= rows || c >= kt * kTcK)
+            continue;
+        uint16_t p[3];
+        split3(tile[i][tx], p[0], p[1], p[2]);
+        const int t = c / kTcK, cc = c % kTcK;
+        uint16_t *o = out + (int64_t)r * op + (int64_t)t * 6 * kTcK + cc;
+#pragma unroll
+        for (int slot = 0; slot < 6; ++slot)
+            o[slot * kTcK] = p[(order >> (2 * slot)) & 3];
+    }
+}
+
+// Xt [K][Tp] = X^T for bf16 X [T][K], zero in the padding (columns T .. Tp).
+__global__ void __launch_bounds__(256)
+    transpose_bf16_kernel(const uint16_t *__restrict__ X, int T, int K, uint16_t *__restrict__ Xt, int Tp)
+{
+    __shared__ uint16_t tile[32][34];
+    const int t0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8) {
+        const int t = t0 + i, kk = k0 + tx;
+        tile[i][tx] = (t < T && kk < K) ? X[(int64_t)t * K + kk] : (uint16_t)0;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int kk = k0 + i, t = t0 + tx;
+        if (kk < K && t < Tp)
+            Xt[(int64_t)kk * Tp + t] = tile[tx][i];
+    }
+}
+
+constexpr uint32_t kOrderA = 0u | (0u << 2) | (1u << 4) | (0u << 6) | (1u << 8) | (2u << 10);  // a0 a0 a1 a0 a1 a2
+constexpr uint32_t kOrderB = 0u | (1u << 2) | (0u << 4) | (2u << 6) | (1u << 8) | (0u << 10);  // b0 b1 b0 b2 b1 b0
+
+nm_status encode_operand(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t kp)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return NM_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)kp, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kp * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? NM_OK
+               : NM_ERR_CUDA;
+}
+
+} // namespace
+
+size_t tc_operand_bytes(int64_t rows, int64_t k, bool emulated)
+{
+    if (emulated && k > 1024) // tc_gemm_f32 splits one chunk of k at a time
+        k = 1024;
+    const int64_t kt = (k + kTcK - 1) / kTcK;
+    return (size_t)rows * kt * kTcK * (emulated ? 6 : 1) * 2;
+}
+
+nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kp, int nparts, float *C, int64_t ldc, int64_t M,
+                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st)
+{
+    if (M <= 0 || N <= 0)
+        return NM_OK;
+    if (kp % kTcK != 0 || N % 4 != 0 || ldc % 4 != 0 || ((uintptr_t)C & 15u) != 0 || M > 0x7FFFFFFF ||
+        N > 0x7FFFFFFF || nparts < 1 || (kp / kTcK) % nparts != 0)
+        return NM_ERR_SHAPE;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    });
+    if (attr != cudaSuccess)
+        return NM_ERR_CUDA;
+    TcMaps maps;
+    nm_status s;
+    if ((s = encode_operand(&maps.a, A, M, kp)) != NM_OK || (s = encode_operand(&maps.b, B, N, kp)) != NM_OK)
+        return s;
+    const dim3 grid((unsigned)((N + kTcN - 1) / kTcN), (unsigned)((M + kTcM - 1) / kTcM));
+    if (grid.y > 65535)
+        return NM_ERR_SHAPE;
+    tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, st>>>(maps, C, ldc, (int)M, (int)N, (int)(kp / kTcK), nparts, alpha,
+                                                        beta, status);
+    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+nm_status tc_split(const float *S, int64_t lds, int64_t rows, int64_t k, bool trans, bool b_side, uint16_t *out,
+                   cudaStream_t st)
+{
+    if (rows <= 0 || k <= 0)
+        return NM_OK;
+    const int64_t kt = (k + kTcK - 1) / kTcK;
+    // the padding columns up to kt * 64 are written as zero parts by the kernel (grid covers them)
+    const dim3 grid((unsigned)((kt * kTcK + 31) / 32), (unsigned)((rows + 31) / 32));
+    split_kernel<<<grid, 256, 0, st>>>(S, lds, (int)rows, (int)k, trans ? 1 : 0, b_side ? kOrderB : kOrderA, out,
+                                       (int)kt);
+    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *Xt, int64_t Tp, cudaStream_t st)
+{
+    if (T <= 0 || K <= 0)
+        return NM_OK;
+    const dim3 grid((unsigned)((K + 31) / 32), (unsigned)((Tp + 31) / 32));
+    transpose_bf16_kernel<<<grid, 256, 0, st>>>(X, (int)T, (int)K, Xt, (int)Tp);
+    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+// ---- plain fp32 on the CUDA cores (the NM_OBS_SGEMM reference mode) -----------
+
+// C = alpha A op(B) + beta C, fp32: A (M x k) row-major; op(B) = B^T for B
+// (N x k) row-major, or B for B (k x N) row-major (b_kn). 64 x 64 outputs per
+// CTA, 4 x 4 per thread, k in steps of 16 through shared memory.
+__global__ void __launch_bounds__(256)
+    simt_gemm_kernel(const float *__restrict__ A, int64_t lda, const float *__restrict__ B, int64_t ldb, int b_kn,
+                     int M, int N, int k, float *C, int64_t ldc, float alpha, float beta)
+{
+    __shared__ float As[16][64 + 4];
+    __shared__ float Bs[16][64 + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < k; k0 += 16) {
+        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+            const int r = i / 16, kk = i % 16; // A tile: row r, column kk
+            As[kk][r] = (m0 + r < M && k0 + kk < k) ? A[(int64_t)(m0 + r) * lda + k0 + kk] : 0.f;
+            if (b_kn) {
+                const int kr = i / 64, c = i % 64; // B rows are k
+                Bs[kr][c] = (n0 + c < N && k0 + kr < k) ? B[(int64_t)(k0 + kr) * ldb + n0 + c] : 0.f;
+            } else {
+                Bs[kk][r] = (n0 + r < N && k0 + kk < k) ? B[(int64_t)(n0 + r) * ldb + k0 + kk] : 0.f;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = As[kk][ty * 4 + i];
+                b[i] = Bs[kk][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = m0 + ty * 4 + i;
+        if (r >= M)
+            continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = n0 + tx * 4 + j;
+            if (c < N) {
+                float *d = C + (int64_t)r * ldc + c;
+                *d = beta != 0.f ? fmaf(beta, *d, alpha * acc[i][j]) : alpha * acc[i][j];
+            }
+        }
+    }
+}
+
+nm_status simt_gemm_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
+                        int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st)
+{
+    if (M <= 0 || N <= 0)
+        return NM_OK;
+    const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
+    if (grid.y > 65535 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || k > 0x7FFFFFFF)
+        return NM_ERR_SHAPE;
+    simt_gemm_kernel<<<grid, 256, 0, st>>>(A, lda, B, ldb, b_kn ? 1 : 0, (int)M, (int)N, (int)(k > 0 ? k : 0), C,
+                                           ldc, alpha, beta);
+    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+}
+
+// The k range of an emulated fp32 GEMM goes through the tensor cores in chunks
+// of kTcChunk, each chunk's result added to C in fp32 (the epilogue's
+// alpha acc + beta C with beta = 1): the tensor cores' accumulation loses more
+// than fp32 rounding over a long k (a Cholesky of K = 14336, with k up to 7168,
+// left more N:M choices off the fp64 oracle's than plain fp32 did).
+constexpr int64_t kTcChunk = 1024;
+
+nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B, int64_t ldb, bool b_trans, int64_t M,
+                      int64_t N, int64_t k, float *C, int64_t ldc, float alpha, float beta, uint16_t *work_a,
+                      uint16_t *work_b, uint32_t *status, cudaStream_t st)
+{
+    if (M <= 0 || N <= 0)
+        return NM_OK;
+    if (k <= 0) // C = beta C
+        return simt_gemm_f32(A, lda, B, ldb, b_trans, M, N, 0, C, ldc, alpha, beta, st);
+    for (int64_t k0 = 0; k0 < k; k0 += kTcChunk) {
+        const int64_t kc = k - k0 < kTcChunk ? k - k0 : kTcChunk;
+        const float *Ak = a_trans ? A + k0 * lda : A + k0;
+        const float *Bk = b_trans ? B + k0 * ldb : B + k0;
+        nm_status s;
+        if ((s = tc_split(Ak, lda, M, kc, a_trans, false, work_a, st)) != NM_OK ||
+            (s = tc_split(Bk, ldb, N, kc, b_trans, true, work_b, st)) != NM_OK)
+            return s;
+        const int64_t kp = ((kc + kTcK - 1) / kTcK) * kTcK * 6;
+        if ((s = tc_gemm_bf16(work_a, work_b, kp, 6, C, ldc, M, N, alpha, k0 == 0 ? beta : 1.0f, status, st)) !=
+            NM_OK)
+            return s;
+    }
+    return NM_OK;
+}
+
+} // namespace nm
