@@ -68,21 +68,31 @@ nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t 
                              const LaunchCtx &ctx);
 
 // ---- tensor-core GEMM of the OBS pruning (tc_gemm.cu) ----
-// C = alpha A B^T + beta C: A bf16 [M][kp], B bf16 [N][kp] (kp a multiple of
-// 64, rows contiguous along k), C fp32 with row stride ldc (16-byte aligned,
-// N and ldc multiples of 4). With nparts > 1 the k-tiles cycle through part
-// slots; slot 0 accumulates apart from the others. A bounded wait that runs
+// Structure flags (coordinates of the GEMM itself: C row i, column j, k
+// index kk): kTcALower: A[i][kk] = 0 for kk > i; kTcBLower: B[j][kk] = 0 for
+// kk > j; kTcBUpper: B[j][kk] = 0 for kk < j (B as the N x k operand);
+// kTcCLower: only the 128 x 128 tiles on and below the diagonal are written
+// (nothing reads the others); kTcCSym: C is symmetric, the tiles on and below
+// the diagonal are computed and the others written as their transposes.
+constexpr unsigned kTcALower = 1u, kTcBLower = 2u, kTcBUpper = 4u, kTcCLower = 8u, kTcCSym = 16u;
+// C = alpha A B^T + beta C: A bf16 [M][kt][nparts][64], B bf16 [N][kt][nparts][64]
+// (nparts 1, or 3 for fp32 emulated: the bf16 parts of each 64-column k-tile
+// side by side), C fp32 with row stride ldc (16-byte aligned, N and ldc
+// multiples of 4). k_base: the global k index of this call's first column,
+// against which the flags' triangles are placed. A bounded wait that runs
 // out sets NM_ERR_TIMEOUT in *status.
-nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kp, int nparts, float *C, int64_t ldc, int64_t M,
-                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st);
+nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kt, int nparts, float *C, int64_t ldc, int64_t M,
+                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st, unsigned flags = 0,
+                       int64_t k_base = 0);
 // fp32 C = alpha A op(B) + beta C with fp32 emulated by bf16 parts (six
 // products): A (M x k) row-major with stride lda (a_trans: stored k x M);
 // op(B) = B^T for B (N x k) row-major, or B for B (k x N) row-major when
 // b_trans. work_a / work_b: tc_operand_bytes(M or N, k, true) bytes each
 // (the k range is done in chunks of 1024, whose results add up in C).
+// flags: as for tc_gemm_bf16, for A and op(B)^T.
 nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B, int64_t ldb, bool b_trans, int64_t M,
                       int64_t N, int64_t k, float *C, int64_t ldc, float alpha, float beta, uint16_t *work_a,
-                      uint16_t *work_b, uint32_t *status, cudaStream_t st);
+                      uint16_t *work_b, uint32_t *status, cudaStream_t st, unsigned flags = 0);
 size_t tc_operand_bytes(int64_t rows, int64_t k, bool emulated);
 // Xt [K][Tp] = X^T (bf16 X [T][K]), zero in columns T .. Tp.
 nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *Xt, int64_t Tp, cudaStream_t st);

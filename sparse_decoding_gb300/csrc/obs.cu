@@ -565,23 +565,27 @@ struct RowGemm {
     uint32_t *status;
     cudaStream_t st;
     // C (M x N) = alpha * A (M x k, stride lda) * op(B) + beta * C (stride ldc);
-    // op(B) = B (k x N) when b_kn, else B^T (B is N x k)
+    // op(B) = B (k x N) when b_kn, else B^T (B is N x k); `tri`: the
+    // structure flags of tc_gemm_f32 (zero or unread parts it may skip)
     bool gemm(int64_t M, int64_t N, int64_t k, float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
-              bool b_kn, float beta, float *C, int64_t ldc) const
+              bool b_kn, float beta, float *C, int64_t ldc, unsigned tri = 0) const
     {
         if (plain)
             return simt_gemm_f32(A, lda, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, st) == NM_OK;
-        return tc_gemm_f32(A, lda, false, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, wa, wb, status, st) == NM_OK;
+        return tc_gemm_f32(A, lda, false, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, wa, wb, status, st, tri) ==
+               NM_OK;
     }
     // C (r x c) = alpha * A (r x k) * B (k x c) + beta * C
-    bool ab(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
+    bool ab(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C,
+            unsigned tri = 0) const
     {
-        return gemm(r, c, k, alpha, A, ld, B, ld, true, beta, C, ld);
+        return gemm(r, c, k, alpha, A, ld, B, ld, true, beta, C, ld, tri);
     }
     // C (r x c) = alpha * A (r x k) * B^T (B is c x k) + beta * C
-    bool abt(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C) const
+    bool abt(int64_t r, int64_t c, int64_t k, float alpha, const float *A, const float *B, float beta, float *C,
+             unsigned tri = 0) const
     {
-        return gemm(r, c, k, alpha, A, ld, B, ld, false, beta, C, ld);
+        return gemm(r, c, k, alpha, A, ld, B, ld, false, beta, C, ld, tri);
     }
 };
 
@@ -618,13 +622,17 @@ bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t
     const int64_t h1 = mid - lo, h2 = hi - mid;
     float *A21 = A + mid * K + lo, *L21 = L + mid * K + lo;
     float *X11 = X + lo * K + lo, *X22 = X + mid * K + mid;
-    if (!chol_inv(G, A, L, X, K, b0, bm, true, not_pd, st) || !G.abt(h2, h1, h1, 1.0f, A21, X11, 0.0f, L21) ||
-        !G.abt(h2, h2, h1, -1.0f, L21, L21, 1.0f, A + mid * K + mid) ||
+    // X11 and X22 are lower triangular, and nothing reads A22 above its
+    // diagonal: the GEMMs skip those zeros and that triangle
+    if (!chol_inv(G, A, L, X, K, b0, bm, true, not_pd, st) ||
+        !G.abt(h2, h1, h1, 1.0f, A21, X11, 0.0f, L21, kTcBLower) ||
+        !G.abt(h2, h2, h1, -1.0f, L21, L21, 1.0f, A + mid * K + mid, kTcCLower) ||
         !chol_inv(G, A, L, X, K, bm, b1, need_x, not_pd, st))
         return false;
     if (!need_x)
         return true;
-    return G.ab(h2, h1, h1, 1.0f, L21, X11, 0.0f, A21) && G.ab(h2, h1, h2, -1.0f, X22, A21, 0.0f, X + mid * K + lo);
+    return G.ab(h2, h1, h1, 1.0f, L21, X11, 0.0f, A21, kTcBUpper) &&
+           G.ab(h2, h1, h2, -1.0f, X22, A21, 0.0f, X + mid * K + lo, kTcALower);
 }
 
 // The sweep's blocks in column order: the factorisation's blocks reversed, so
@@ -749,8 +757,9 @@ extern "C" nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, fl
     std::lock_guard<std::mutex> lock(g_obs_mu);
     // H[i][j] = 2 sum_t X[t][i] X[t][j]: X^T (bf16 [K][Tp], t contiguous, zero
     // padding to a multiple of 64 tokens) is both operands of one bf16 pass;
-    // the products are exact and the sums fp32. A bounded wait that runs out
-    // is reported by nm_device_status.
+    // the products are exact and the sums fp32. H is symmetric: the tiles on
+    // and below the diagonal are computed and mirrored. A bounded wait that
+    // runs out is reported by nm_device_status.
     uint32_t *status = nullptr;
     nm_status s = library_status_word(&status);
     if (s != NM_OK)
@@ -762,7 +771,7 @@ extern "C" nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, fl
     uint16_t *Xt = (uint16_t *)ws.p;
     if ((s = tc_transpose_bf16((const uint16_t *)X_bf16, T, K, Xt, Tp, st)) != NM_OK)
         return s;
-    return tc_gemm_bf16(Xt, Xt, Tp, 1, H, K, K, K, 2.0f, accumulate ? 1.0f : 0.0f, status, st);
+    return tc_gemm_bf16(Xt, Xt, Tp / 64, 1, H, K, K, K, 2.0f, accumulate ? 1.0f : 0.0f, status, st, kTcCSym);
 }
 
 extern "C" nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t rows, int64_t K, int N, int M,

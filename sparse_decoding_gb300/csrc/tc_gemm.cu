@@ -5,31 +5,38 @@
 //   C = alpha * A * B^T + beta * C     A: bf16 [M][k], B: bf16 [N][k] (rows
 //                                      contiguous along k), C: fp32 [M][N]
 //
-// One CTA computes a 128 x 128 tile of C: warp 0 (one thread) streams 64-wide
-// k-tiles of A and B into a ring of shared-memory stages by TMA (128-byte
-// swizzle); warp 1 (one thread) issues four M=128, N=128, K=16 tcgen05.mma per
-// stage into 128-column fp32 accumulators in tensor memory (four of them, see
-// below) and releases the stage with tcgen05.commit; at the end all four warps
-// read the accumulators with tcgen05.ld (warp w: rows 32w..32w+31, one row per
-// thread), add them, and write C.
+// One CTA computes a 128 x 128 tile of C: warp 0 (one thread) streams k-tiles
+// of A and B into a ring of shared-memory stages by TMA; warp 1 (one thread)
+// issues M=128, N=128, K=16 tcgen05.mma into 128-column fp32 accumulators in
+// tensor memory (four of them, see below) and releases each stage with
+// tcgen05.commit; at the end all four warps read the accumulators with
+// tcgen05.ld (warp w: rows 32w..32w+31, one row per thread), add them, and
+// write C.
 //
 // fp32 products (the Cholesky steps and the lazy update) are emulated with
 // bf16 parts: a = a0 + a1 + a2 with a0 = bf16(a), a1 = bf16(a - a0),
 // a2 = bf16(a - a0 - a1) (together 24 bits of a's significand), and
 //   a b ~ a0 b0 + a0 b1 + a1 b0 + a0 b2 + a1 b1 + a2 b0
 // -- every product of order up to 2 -- accumulated in fp32; the dropped terms
-// are below 2^-24 |a b|. split_kernel writes the parts of a fp32 matrix as one
-// bf16 operand whose k dimension interleaves them per 64-column tile (A side:
-// a0 a0 a1 a0 a1 a2; B side: b0 b1 b0 b2 b1 b0), so that one bf16 GEMM over a
-// six times longer k forms exactly those six products. The leading products
-// a0 b0 of successive k-tiles take turns in three tensor-memory accumulators
-// and the five smaller ones go to a fourth; the four are added once at the
-// end, in a fixed order. The tensor cores' accumulation loses more than fp32
-// rounding as k grows (in one accumulator, the mean error at k = 2048 was 2.8
-// times that of fp32 on the CUDA cores); spreading k over several
-// accumulators keeps each sum shorter. The Hessian's operand (bf16
-// calibration inputs, transposed) needs one part: its products are exact, and
+// are below 2^-24 |a b|. split_kernel writes the three parts of a fp32 matrix
+// side by side per 64-column k-tile ([rows][k-tiles][part][64] bf16, the same
+// layout for A and B), so a pipeline stage holds the three part tiles of A
+// and of B for a slice of k, and the six products are six groups of MMAs on
+// them: every operand byte crosses from L2 to shared memory once. The leading
+// products a0 b0 of successive k-tiles take turns in three tensor-memory
+// accumulators and the five smaller ones go to a fourth; the four are added
+// once at the end, in a fixed order. The tensor cores' accumulation loses
+// more than fp32 rounding as k grows (in one accumulator, the mean error at
+// k = 2048 was 2.8 times that of fp32 on the CUDA cores); spreading k over
+// several accumulators keeps each sum shorter. The Hessian's operand (bf16
+// calibration inputs, transposed) has one part: its products are exact, and
 // its k-tiles take turns in all four accumulators.
+//
+// Structure flags skip what is known to be zero or not needed: a triangular
+// operand limits each tile's k range, a C whose upper part nobody reads
+// skips the tiles above the diagonal, and a symmetric C computes the tiles on
+// and below the diagonal and writes each off-diagonal one twice (once
+// transposed, which stays coalesced: lanes hold consecutive rows).
 //
 // Every wait is bounded (about a second); a wait that runs out sets a flag the
 // host reads, and the kernel still frees its tensor memory and returns.
@@ -46,12 +53,22 @@ namespace {
 
 constexpr int kTcM = 128;        // rows of C per CTA (tensor-memory lanes)
 constexpr int kTcN = 128;        // columns of C per CTA (tensor-memory columns)
-constexpr int kTcK = 64;         // k per stage: one 128-byte swizzled row of bf16
-constexpr int kTcStages = 4;
-constexpr int kTcTileBytes = kTcM * kTcK * 2;              // 16 KB (A; B is the same)
-constexpr int kTcStageBytes = 2 * kTcTileBytes;            // A + B
-constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024;  // + alignment slack
+constexpr int kTcK = 64;         // k per part tile in the operand layout
 constexpr int kTcThreads = 128;
+constexpr int kTcAcc = 4;        // 128-column accumulators (all 512 tensor-memory columns)
+
+// A pipeline stage holds NP part tiles of A and NP of B, each KW columns of
+// k wide (KW = 64: 128-byte rows, 128-byte swizzle; KW = 32: 64-byte rows,
+// 64-byte swizzle), in a ring of S stages.
+template <int NP, int KW> struct TcCfg {
+    static constexpr int kTile = kTcM * KW * 2;                    // bytes of one part tile
+    static constexpr int kStage = 2 * NP * kTile;
+    static constexpr int kStages = (192 * 1024) / kStage;          // 2..12
+    static constexpr int kSmem = kStages * kStage + 1024;          // + alignment slack
+    static constexpr int kSub = kTcK / KW;                         // stages per 64-wide k-tile
+    static constexpr int kSlices = KW / 16;                        // K=16 MMAs per part pair and stage
+    static constexpr int kSwizzleBytes = KW * 2;
+};
 
 // ---- tensor-memory and tensor-core instructions (PTX ISA, tcgen05) ----------
 
@@ -99,20 +116,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (the
-// stride byte offset), start address in 16-byte units, descriptor version 1,
-// layout type 2 (128-byte swizzle). The leading byte offset is not used by
-// this layout. The tile starts on a 1024-byte boundary (base offset 0); a
-// k-slice of 16 elements inside it starts 32 bytes further per slice.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+// Shared-memory matrix descriptor of a K-major tile written by TMA with a
+// SW-byte swizzle (SW = 128 or 64): rows of SW bytes, 8-row groups 8 SW
+// bytes apart (the stride byte offset), start address in 16-byte units,
+// descriptor version 1, layout type 2 (128-byte swizzle) or 4 (64-byte). The
+// leading byte offset is not used by these layouts. The tile starts on a
+// 1024-byte boundary (base offset 0); a k-slice of 16 elements inside it
+// starts 32 bytes further per slice.
+template <int SW> __device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr)
 {
+    static_assert(SW == 128 || SW == 64, "swizzle width");
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;            // leading byte offset (unused): 16 bytes
-    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 1024 bytes
-    d |= (uint64_t)1 << 46;            // descriptor version
-    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused): 16 bytes
+    d |= (uint64_t)((8 * SW) >> 4) << 32;       // stride byte offset: 8 rows
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)(SW == 128 ? 2 : 4) << 61;   // swizzle mode
     return d;
 }
 
@@ -138,50 +157,117 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     return true;
 }
 
-// The accumulator of k-tile t (a) and whether t is the first tile it gets.
-// One part (nparts == 1): tiles take turns in all four accumulators. Several
-// (fp32 emulated): tile t holds part slot t % nparts; slot 0, the leading
-// products, takes turns in accumulators 0..2 by part group t / nparts, and
-// the other slots all go to accumulator 3 (first used by tile 1).
-constexpr int kTcAcc = 4;
-__device__ __forceinline__ void tc_route(int t, int nparts, int &a, bool &first)
+// The products of one k-tile with three parts, leading one first:
+// a0 b0, a0 b1, a1 b0, a0 b2, a1 b1, a2 b0 (two bits per product: the part).
+constexpr uint32_t kPartA = 0u | (0u << 2) | (1u << 4) | (0u << 6) | (1u << 8) | (2u << 10);
+constexpr uint32_t kPartB = 0u | (1u << 2) | (0u << 4) | (2u << 6) | (1u << 8) | (0u << 10);
+template <int NP> constexpr int kProducts = NP == 1 ? 1 : 6;
+
+// The accumulator of product q of the tile's u-th 64-wide k-tile. One part:
+// the k-tiles take turns in all four. Three: the leading products take turns
+// in accumulators 0..2, the other five all go to accumulator 3.
+__host__ __device__ constexpr int tc_acc(int u, int q, int np)
 {
-    if (nparts == 1) {
-        a = t % kTcAcc;
-        first = t < kTcAcc;
-        return;
-    }
-    const int slot = t % nparts, group = t / nparts;
-    if (slot == 0) {
-        a = group % (kTcAcc - 1);
-        first = group < kTcAcc - 1;
-    } else {
-        a = kTcAcc - 1;
-        first = t == 1;
-    }
+    return np == 1 ? u % kTcAcc : (q == 0 ? u % (kTcAcc - 1) : kTcAcc - 1);
+}
+// The accumulators that receive a product when a tile runs n k-tiles.
+__device__ __forceinline__ uint32_t tc_used(int n, int np)
+{
+    if (n <= 0)
+        return 0;
+    if (np == 1)
+        return (1u << (n < kTcAcc ? n : kTcAcc)) - 1;
+    return ((1u << (n < kTcAcc - 1 ? n : kTcAcc - 1)) - 1) | (1u << (kTcAcc - 1));
 }
 
 struct TcMaps {
-    CUtensorMap a;  // bf16 [M][kp], box 64 x 128, 128-byte swizzle
-    CUtensorMap b;  // bf16 [N][kp], box 64 x 128, 128-byte swizzle
+    CUtensorMap a;  // bf16 [M][kt * NP * 64], box KW x 128
+    CUtensorMap b;  // bf16 [N][kt * NP * 64], box KW x 128
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ TcMaps maps, float *C, int64_t ldc, int M, int N, int ktiles, int nparts,
-                   float alpha, float beta, uint32_t *err)
+// One 32-column slice of a finished tile row: C[row][n0+c ..] = alpha v +
+// beta C (v = 0 when the tile had no k range), and with `mirror` also
+// C[n0+c+j][row] (the transposed tile; lanes hold consecutive rows, so each
+// of those 32 stores is one coalesced 128-byte line).
+__device__ __forceinline__ void tc_store32(float *C, int64_t ldc, int row, int col, int M, int N, const float (&v)[32],
+                                           float alpha, float beta, bool mirror)
 {
-    __shared__ __align__(8) uint64_t full_bar[kTcStages];
-    __shared__ __align__(8) uint64_t empty_bar[kTcStages];
+    if (row >= M || col >= N)
+        return;
+    float *dst = C + (int64_t)row * ldc + col;
+    const int ncol = N - col < 32 ? N - col : 32; // a multiple of 4
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        if (j < ncol) {
+            float4 o = make_float4(alpha * v[j], alpha * v[j + 1], alpha * v[j + 2], alpha * v[j + 3]);
+            if (beta != 0.f) {
+                const float4 c = *(const float4 *)(dst + j);
+                o.x = fmaf(beta, c.x, o.x);
+                o.y = fmaf(beta, c.y, o.y);
+                o.z = fmaf(beta, c.z, o.z);
+                o.w = fmaf(beta, c.w, o.w);
+            }
+            *(float4 *)(dst + j) = o;
+        }
+    }
+    if (mirror) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+                float *t = C + (int64_t)(col + j) * ldc + row;
+                *t = beta != 0.f ? fmaf(beta, *t, alpha * v[j]) : alpha * v[j];
+            }
+        }
+    }
+}
+
+template <int NP, int KW>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, float *C, int64_t ldc, int M, int N, int ktiles,
+                   int64_t k_base, uint32_t flags, float alpha, float beta, uint32_t *err)
+{
+    using Cfg = TcCfg<NP, KW>;
+    constexpr int S = Cfg::kStages;
+    const int n0 = blockIdx.x * kTcN, m0 = blockIdx.y * kTcM;
+    if ((flags & (kTcCLower | kTcCSym)) && blockIdx.x > blockIdx.y)
+        return;  // above the diagonal: not needed, or written by the mirror tile
+    const bool mirror = (flags & kTcCSym) && blockIdx.x < blockIdx.y;
+    // this tile's 64-wide k-tiles [t_lo, t_hi) (global k = k_base + 64 t)
+    int64_t lo = k_base, hi = k_base + (int64_t)ktiles * kTcK;
+    if ((flags & kTcALower) && hi > (int64_t)m0 + kTcM)
+        hi = (int64_t)m0 + kTcM;
+    if ((flags & kTcBLower) && hi > (int64_t)n0 + kTcN)
+        hi = (int64_t)n0 + kTcN;
+    if ((flags & kTcBUpper) && lo < (int64_t)n0)
+        lo = (int64_t)n0;
+    const int t_lo = lo < hi ? (int)((lo - k_base) / kTcK) : 0;
+    const int t_hi = lo < hi ? (int)((hi - k_base + kTcK - 1) / kTcK) : 0;
+    const int nt = t_hi - t_lo;              // uniform over the CTA
+    const int nstage = nt * Cfg::kSub;       // pipeline stages of this tile
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = m0 + warp * 32 + lane;
+
+    if (nt == 0) {
+        // no k range: C = beta C (nothing to do when beta is 1)
+        if (beta != 1.0f) {
+            const float zero[32] = {};
+#pragma unroll 1
+            for (int c = 0; c < kTcN; c += 32)
+                tc_store32(C, ldc, row, n0 + c, M, N, zero, alpha, beta, mirror);
+        }
+        return;
+    }
+
+    __shared__ __align__(8) uint64_t full_bar[S];
+    __shared__ __align__(8) uint64_t empty_bar[S];
     __shared__ __align__(8) uint64_t done_bar;
     __shared__ uint32_t tmem_base;
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *const tiles = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
     const uint32_t tiles0 = smem_addr(tiles);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTcN, m0 = blockIdx.y * kTcM;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1);
             mbar_init(smem_addr(&empty_bar[s]), 1);
         }
@@ -196,60 +282,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = tmem_base;
 
     if (warp == 0 && lane == 0) {
-        // producer: k-tile t goes to stage t % S, once the MMAs of tile t - S have released it
+        // producer: stage i (k-tile t_lo + i / kSub, sub-slice i % kSub) goes
+        // to slot i % S once the MMAs of stage i - S have released it
         int issued = 0;
-        for (int t = 0; t < ktiles; ++t) {
-            const int s = t % kTcStages;
-            if (t >= kTcStages && !wait_bounded(smem_addr(&empty_bar[s]), ((t / kTcStages) - 1) & 1, err))
+        for (int i = 0; i < nstage; ++i) {
+            const int s = i % S;
+            if (i >= S && !wait_bounded(smem_addr(&empty_bar[s]), ((i / S) - 1) & 1, err))
                 break;
             const uint32_t fb = smem_addr(&full_bar[s]);
-            mbar_arrive_expect_tx(fb, kTcStageBytes);
-            const uint32_t sa = tiles0 + s * kTcStageBytes;
-            tma_load_2d(sa, &maps.a, t * kTcK, m0, fb);
-            tma_load_2d(sa + kTcTileBytes, &maps.b, t * kTcK, n0, fb);
-            issued = t + 1;
+            mbar_arrive_expect_tx(fb, Cfg::kStage);
+            const uint32_t sa = tiles0 + s * Cfg::kStage;
+            const int t = t_lo + i / Cfg::kSub, x0 = (i % Cfg::kSub) * KW;
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                const int x = (t * NP + p) * kTcK + x0;
+                tma_load_2d(sa + p * Cfg::kTile, &maps.a, x, m0, fb);
+                tma_load_2d(sa + (NP + p) * Cfg::kTile, &maps.b, x, n0, fb);
+            }
+            issued = i + 1;
         }
         // before leaving, let the copies that may still be in flight land (bounded)
-        for (int t = issued - kTcStages > 0 ? issued - kTcStages : 0; t < issued; ++t)
-            if (!wait_bounded(smem_addr(&full_bar[t % kTcStages]), (t / kTcStages) & 1, err))
+        for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
+            if (!wait_bounded(smem_addr(&full_bar[i % S]), (i / S) & 1, err))
                 break;
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
-        bool ok = true;
-        for (int t = 0; t < ktiles && ok; ++t) {
-            const int s = t % kTcStages;
-            ok = wait_bounded(smem_addr(&full_bar[s]), (t / kTcStages) & 1, err);
-            if (!ok)
+        uint32_t touched = 0;
+        for (int i = 0; i < nstage; ++i) {
+            const int s = i % S;
+            if (!wait_bounded(smem_addr(&full_bar[s]), (i / S) & 1, err))
                 break;
             tc_fence_after();
-            const uint32_t sa = tiles0 + s * kTcStageBytes;
-            int a;
-            bool first;
-            tc_route(t, nparts, a, first);
-            const uint32_t acc = tmem + (uint32_t)(a * kTcN);
+            const uint32_t sa = tiles0 + s * Cfg::kStage, sb = sa + NP * Cfg::kTile;
+            const int u = i / Cfg::kSub;
 #pragma unroll
-            for (int k = 0; k < kTcK / 16; ++k) {
-                const uint64_t ad = smem_desc_sw128(sa + k * 32);
-                const uint64_t bd = smem_desc_sw128(sa + kTcTileBytes + k * 32);
-                tc_mma_bf16(acc, ad, bd, kIdescBf16, (first && k == 0) ? 0u : 1u);
+            for (int q = 0; q < kProducts<NP>; ++q) {
+                const int pa = (kPartA >> (2 * q)) & 3, pb = (kPartB >> (2 * q)) & 3;
+                const int a = tc_acc(u, q, NP);
+                const uint32_t acc = tmem + (uint32_t)(a * kTcN);
+#pragma unroll
+                for (int k = 0; k < Cfg::kSlices; ++k) {
+                    const uint64_t ad = smem_desc_sw<Cfg::kSwizzleBytes>(sa + pa * Cfg::kTile + k * 32);
+                    const uint64_t bd = smem_desc_sw<Cfg::kSwizzleBytes>(sb + pb * Cfg::kTile + k * 32);
+                    tc_mma_bf16(acc, ad, bd, kIdescBf16, ((touched >> a) & 1u) | (k > 0 ? 1u : 0u));
+                }
+                touched |= 1u << a;
             }
             tc_commit(smem_addr(&empty_bar[s])); // the stage is free once these MMAs are done
         }
-        tc_commit(smem_addr(&done_bar)); // the accumulator is complete once every MMA is done
+        tc_commit(smem_addr(&done_bar)); // the accumulators are complete once every MMA is done
     }
     __syncwarp();
-    // epilogue: every warp waits for the accumulator, then reads its 32 lanes
-    const bool have = wait_bounded(smem_addr(&done_bar), 0, err) && ktiles > 0;
+    // epilogue: every warp waits for the accumulators, then reads its 32 lanes
+    const bool have = wait_bounded(smem_addr(&done_bar), 0, err);
     tc_fence_after();
-    const int row = m0 + warp * 32 + lane;
-    // the accumulators that received a k-tile, added in index order
-    uint32_t used = 0;
-    for (int t = 0; t < ktiles && t < 4 * nparts; ++t) {
-        int a;
-        bool first;
-        tc_route(t, nparts, a, first);
-        used |= 1u << a;
-    }
+    const uint32_t used = tc_used(nt, NP);
 #pragma unroll 1
     for (int c = 0; c < kTcN; c += 32) {
         uint32_t r[32];
@@ -264,28 +351,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int j = 0; j < 32; ++j)
                 r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
         }
-        if (row >= M || n0 + c >= N)
-            continue;
-        float *dst = C + (int64_t)row * ldc + n0 + c;
-        const int ncol = N - (n0 + c) < 32 ? N - (n0 + c) : 32; // a multiple of 4
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            if (j < ncol) {
-                float4 v;
-                v.x = have ? alpha * __uint_as_float(r[j]) : 0.f;
-                v.y = have ? alpha * __uint_as_float(r[j + 1]) : 0.f;
-                v.z = have ? alpha * __uint_as_float(r[j + 2]) : 0.f;
-                v.w = have ? alpha * __uint_as_float(r[j + 3]) : 0.f;
-                if (beta != 0.f) {
-                    const float4 o = *(const float4 *)(dst + j);
-                    v.x = fmaf(beta, o.x, v.x);
-                    v.y = fmaf(beta, o.y, v.y);
-                    v.z = fmaf(beta, o.z, v.z);
-                    v.w = fmaf(beta, o.w, v.w);
-                }
-                *(float4 *)(dst + j) = v;
-            }
-        }
+        for (int j = 0; j < 32; ++j)
+            v[j] = have ? __uint_as_float(r[j]) : 0.0f;
+        tc_store32(C, ldc, row, n0 + c, M, N, v, alpha, beta, mirror);
     }
     tc_fence_before();
     __syncthreads();
@@ -306,18 +376,16 @@ __device__ __forceinline__ void split3(float a, uint16_t &p0, uint16_t &p1, uint
     p2 = f32_to_bf16_rn(r2);
 }
 
-// Out [rows][kt * 6 * 64] bf16: for row r and k-tile t, six 64-wide slots of
-// parts of S's elements (r, 64 t .. 64 t + 63) in the order `order` (two bits
-// per slot: the part index), zero beyond k or rows. S is fp32 with row stride
+// Out [rows][kt][3][64] bf16: for row r and k-tile t, the three parts of S's
+// elements (r, 64 t .. 64 t + 63), zero beyond k. S is fp32 with row stride
 // lds, read as S[r][c] or, transposed, as S[c][r]. A CTA covers 32 rows x 32
 // columns through a shared tile (the transposed read stays coalesced).
 __global__ void __launch_bounds__(256)
-    split_kernel(const float *__restrict__ S, int64_t lds, int rows, int k, int trans, uint32_t order,
-                 uint16_t *__restrict__ out, int kt)
+    split_kernel(const float *__restrict__ S, int64_t lds, int rows, int k, int trans, uint16_t *__restrict__ out,
+                 int kt)
 {
     __shared__ float tile[32][33];
-    const int64_t op = (int64_t)kt * 6 * kTcK; // out row pitch (elements)
-    // blocks cover 32 rows x 32 source columns
+    const int64_t op = (int64_t)kt * 3 * kTcK; // out row pitch (elements)
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5; // 32 x 8
     for (int i = ty; i < 32; i += 8) {
@@ -340,13 +408,12 @@ __global__ void __launch_bounds__(256)
         const int r = r0 + i, c = c0 + tx;
         if (r >= rows || c >= kt * kTcK)
             continue;
-        uint16_t p[3];
-        split3(tile[i][tx], p[0], p[1], p[2]);
-        const int t = c / kTcK, cc = c % kTcK;
-        uint16_t *o = out + (int64_t)r * op + (int64_t)t * 6 * kTcK + cc;
-#pragma unroll
-        for (int slot = 0; slot < 6; ++slot)
-            o[slot * kTcK] = p[(order >> (2 * slot)) & 3];
+        uint16_t p0, p1, p2;
+        split3(tile[i][tx], p0, p1, p2);
+        uint16_t *o = out + (int64_t)r * op + (int64_t)(c / kTcK) * 3 * kTcK + c % kTcK;
+        o[0] = p0;
+        o[kTcK] = p1;
+        o[2 * kTcK] = p2;
     }
 }
 
@@ -369,23 +436,46 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-constexpr uint32_t kOrderA = 0u | (0u << 2) | (1u << 4) | (0u << 6) | (1u << 8) | (2u << 10);  // a0 a0 a1 a0 a1 a2
-constexpr uint32_t kOrderB = 0u | (1u << 2) | (0u << 4) | (2u << 6) | (1u << 8) | (0u << 10);  // b0 b1 b0 b2 b1 b0
-
-nm_status encode_operand(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t kp)
+template <int KW> nm_status encode_operand(CUtensorMap *map, const uint16_t *ptr, int64_t rows, int64_t pitch)
 {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn)
         return NM_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)kp, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kp * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcM};
+    const cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)KW, (cuuint32_t)kTcM};
     const cuuint32_t es[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+              CU_TENSOR_MAP_INTERLEAVE_NONE, KW == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
                ? NM_OK
                : NM_ERR_CUDA;
+}
+
+template <int NP, int KW>
+nm_status launch_tc(const uint16_t *A, const uint16_t *B, int64_t kt, float *C, int64_t ldc, int64_t M, int64_t N,
+                    int64_t k_base, uint32_t flags, float alpha, float beta, uint32_t *status, cudaStream_t st)
+{
+    using Cfg = TcCfg<NP, KW>;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(tc_gemm_kernel<NP, KW>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    });
+    if (attr != cudaSuccess)
+        return NM_ERR_CUDA;
+    TcMaps maps;
+    nm_status s;
+    const int64_t pitch = kt * NP * kTcK;
+    if ((s = encode_operand<KW>(&maps.a, A, M, pitch)) != NM_OK ||
+        (s = encode_operand<KW>(&maps.b, B, N, pitch)) != NM_OK)
+        return s;
+    const dim3 grid((unsigned)((N + kTcN - 1) / kTcN), (unsigned)((M + kTcM - 1) / kTcM));
+    if (grid.y > 65535)
+        return NM_ERR_SHAPE;
+    tc_gemm_kernel<NP, KW><<<grid, kTcThreads, Cfg::kSmem, st>>>(maps, C, ldc, (int)M, (int)N, (int)kt, k_base, flags,
+                                                                 alpha, beta, status);
+    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
 } // namespace
@@ -395,46 +485,31 @@ size_t tc_operand_bytes(int64_t rows, int64_t k, bool emulated)
     if (emulated && k > 1024) // tc_gemm_f32 splits one chunk of k at a time
         k = 1024;
     const int64_t kt = (k + kTcK - 1) / kTcK;
-    return (size_t)rows * kt * kTcK * (emulated ? 6 : 1) * 2;
+    return (size_t)rows * kt * kTcK * (emulated ? 3 : 1) * 2;
 }
 
-nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kp, int nparts, float *C, int64_t ldc, int64_t M,
-                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st)
+nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kt, int nparts, float *C, int64_t ldc, int64_t M,
+                       int64_t N, float alpha, float beta, uint32_t *status, cudaStream_t st, unsigned flags,
+                       int64_t k_base)
 {
     if (M <= 0 || N <= 0)
         return NM_OK;
-    if (kp % kTcK != 0 || N % 4 != 0 || ldc % 4 != 0 || ((uintptr_t)C & 15u) != 0 || M > 0x7FFFFFFF ||
-        N > 0x7FFFFFFF || nparts < 1 || (kp / kTcK) % nparts != 0)
+    if (kt < 0 || kt * nparts * kTcK > 0x7FFFFFFF || N % 4 != 0 || ldc % 4 != 0 || ((uintptr_t)C & 15u) != 0 ||
+        M > 0x7FFFFFFF || N > 0x7FFFFFFF || (nparts != 1 && nparts != 3) ||
+        ((flags & (kTcCLower | kTcCSym)) && M != N))
         return NM_ERR_SHAPE;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-    });
-    if (attr != cudaSuccess)
-        return NM_ERR_CUDA;
-    TcMaps maps;
-    nm_status s;
-    if ((s = encode_operand(&maps.a, A, M, kp)) != NM_OK || (s = encode_operand(&maps.b, B, N, kp)) != NM_OK)
-        return s;
-    const dim3 grid((unsigned)((N + kTcN - 1) / kTcN), (unsigned)((M + kTcM - 1) / kTcM));
-    if (grid.y > 65535)
-        return NM_ERR_SHAPE;
-    tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, st>>>(maps, C, ldc, (int)M, (int)N, (int)(kp / kTcK), nparts, alpha,
-                                                        beta, status);
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    return nparts == 1 ? launch_tc<1, 64>(A, B, kt, C, ldc, M, N, k_base, flags, alpha, beta, status, st)
+                       : launch_tc<3, 32>(A, B, kt, C, ldc, M, N, k_base, flags, alpha, beta, status, st);
 }
 
-nm_status tc_split(const float *S, int64_t lds, int64_t rows, int64_t k, bool trans, bool b_side, uint16_t *out,
-                   cudaStream_t st)
+nm_status tc_split(const float *S, int64_t lds, int64_t rows, int64_t k, bool trans, uint16_t *out, cudaStream_t st)
 {
     if (rows <= 0 || k <= 0)
         return NM_OK;
     const int64_t kt = (k + kTcK - 1) / kTcK;
     // the padding columns up to kt * 64 are written as zero parts by the kernel (grid covers them)
     const dim3 grid((unsigned)((kt * kTcK + 31) / 32), (unsigned)((rows + 31) / 32));
-    split_kernel<<<grid, 256, 0, st>>>(S, lds, (int)rows, (int)k, trans ? 1 : 0, b_side ? kOrderB : kOrderA, out,
-                                       (int)kt);
+    split_kernel<<<grid, 256, 0, st>>>(S, lds, (int)rows, (int)k, trans ? 1 : 0, out, (int)kt);
     return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
@@ -527,23 +602,27 @@ constexpr int64_t kTcChunk = 1024;
 
 nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B, int64_t ldb, bool b_trans, int64_t M,
                       int64_t N, int64_t k, float *C, int64_t ldc, float alpha, float beta, uint16_t *work_a,
-                      uint16_t *work_b, uint32_t *status, cudaStream_t st)
+                      uint16_t *work_b, uint32_t *status, cudaStream_t st, unsigned flags)
 {
     if (M <= 0 || N <= 0)
         return NM_OK;
     if (k <= 0) // C = beta C
         return simt_gemm_f32(A, lda, B, ldb, b_trans, M, N, 0, C, ldc, alpha, beta, st);
+    // B is A (the product of a matrix with its own transpose): one split serves both
+    const bool same = A == B && a_trans == b_trans && lda == ldb && M == N;
     for (int64_t k0 = 0; k0 < k; k0 += kTcChunk) {
         const int64_t kc = k - k0 < kTcChunk ? k - k0 : kTcChunk;
+        // a chunk that no tile's k range reaches leaves C as it is (beta is 1 after the first)
+        if (k0 > 0 && (((flags & kTcALower) && k0 >= M) || ((flags & kTcBLower) && k0 >= N)))
+            break;
         const float *Ak = a_trans ? A + k0 * lda : A + k0;
         const float *Bk = b_trans ? B + k0 * ldb : B + k0;
         nm_status s;
-        if ((s = tc_split(Ak, lda, M, kc, a_trans, false, work_a, st)) != NM_OK ||
-            (s = tc_split(Bk, ldb, N, kc, b_trans, true, work_b, st)) != NM_OK)
+        if ((s = tc_split(Ak, lda, M, kc, a_trans, work_a, st)) != NM_OK ||
+            (!same && (s = tc_split(Bk, ldb, N, kc, b_trans, work_b, st)) != NM_OK))
             return s;
-        const int64_t kp = ((kc + kTcK - 1) / kTcK) * kTcK * 6;
-        if ((s = tc_gemm_bf16(work_a, work_b, kp, 6, C, ldc, M, N, alpha, k0 == 0 ? beta : 1.0f, status, st)) !=
-            NM_OK)
+        if ((s = tc_gemm_bf16(work_a, same ? work_a : work_b, (kc + kTcK - 1) / kTcK, 3, C, ldc, M, N, alpha,
+                              k0 == 0 ? beta : 1.0f, status, st, flags, k0)) != NM_OK)
             return s;
     }
     return NM_OK;
