@@ -372,9 +372,11 @@ nm_status nm_device_status(void *stream);
  *     and its weights 0, then percdamp * mean(diag H) is added to the diagonal.
  */
 
-/* Flag of nm_obs_prune: the factorisations and the lazy trailing updates run in
- * plain fp32 instead of fp32 emulated on the bf16 tensor cores (each operand
- * split into 3 bf16 terms; the default). */
+/* Flag of nm_obs_prune: the GEMM-shaped steps (the factorisation's off-diagonal
+ * blocks and the lazy trailing updates) run in plain fp32 on the CUDA cores
+ * instead of fp32 emulated on the bf16 tensor cores (the default: each fp32
+ * operand split into three bf16 parts, the six products of order up to 2
+ * accumulated in fp32 in tensor memory, k in chunks of 1024 added in fp32). */
 #define NM_OBS_SGEMM 1u
 
 /*
@@ -382,9 +384,12 @@ nm_status nm_device_status(void *stream);
  *   X_bf16 : device, bf16 [T][K], one row per calibration token (read).
  *   H      : device, fp32 [K][K], symmetric (written; accumulated into when
  *            `accumulate` is nonzero, so long calibration sets go in chunks).
- * Products are exact; sums are fp32. T == 0 writes zeros (or leaves H as it
- * is when accumulating). K must be a multiple of 32; T and K at most 2^31 - 1.
- * Asynchronous on `stream`. Calls on one device are serialized by a lock.
+ * Products are exact; sums are fp32 (one bf16 pass on the tensor cores; the
+ * tiles on and below the diagonal are computed and mirrored). T == 0 writes
+ * zeros (or leaves H as it is when accumulating). K must be a multiple of 32;
+ * T and K at most 2^31 - 1. Workspace: X transposed, 2 K ceil(T/64)*64 bytes
+ * from the stream-ordered allocator. Asynchronous on `stream`. Calls on one
+ * device are serialized by a lock.
  */
 nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int accumulate, void *stream);
 
@@ -405,10 +410,12 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  *   W_out_f32   : device, fp32 [rows][K] or NULL (written): the pruned weights
  *                 in fp32, before the rounding to bf16.
  * Arithmetic is fp32: the Cholesky factorisation of the reversed Hessian, the
- * inverses it needs and the column sweep run in this library's kernels, their
- * GEMM-shaped steps in cuBLAS. Workspace: 12 K^2 + 4 rows K + 4096 rows
- * bytes, taken from the stream-ordered allocator and returned before the call
- * ends. SYNCHRONOUS: returns after the result is written (NM_ERR_NOT_PD when
+ * inverses it needs, the column sweep and the GEMM-shaped steps all run in
+ * this library's kernels (the GEMMs on the tensor cores with fp32 emulated,
+ * see NM_OBS_SGEMM). Workspace: 12 K^2 + 4 rows K + 4096 rows bytes, plus
+ * 6144 (max(rows, K/2) + K) bytes for the GEMMs' split operands (none with
+ * NM_OBS_SGEMM), taken from the stream-ordered allocator and returned before
+ * the call ends. SYNCHRONOUS: returns after the result is written (NM_ERR_NOT_PD when
  * the damped Hessian cannot be factorised; outputs are then unspecified).
  * Calls on one device are serialized by a lock. Pointers 16-byte aligned
  * (NM_ERR_ALIGN).
