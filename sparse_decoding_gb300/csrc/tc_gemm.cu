@@ -376,17 +376,32 @@ __device__ __forceinline__ void split3(float a, uint16_t &p0, uint16_t &p1, uint
     p2 = f32_to_bf16_rn(r2);
 }
 
+// One operand to split: S fp32 with row stride lds, read as S[r][c] (or,
+// transposed, S[c][r]) for rows x k, into out.
+struct SplitOp {
+    const float *S;
+    int64_t lds;
+    int rows, trans;
+    uint16_t *out;
+};
+
 // Out [rows][kt][3][64] bf16: for row r and k-tile t, the three parts of S's
-// elements (r, 64 t .. 64 t + 63), zero beyond k. S is fp32 with row stride
-// lds, read as S[r][c] or, transposed, as S[c][r]. A CTA covers 32 rows x 32
-// columns through a shared tile (the transposed read stays coalesced).
-__global__ void __launch_bounds__(256)
-    split_kernel(const float *__restrict__ S, int64_t lds, int rows, int k, int trans, uint16_t *__restrict__ out,
-                 int kt)
+// elements (r, 64 t .. 64 t + 63), zero beyond k. A CTA covers 32 rows x 32
+// columns through a shared tile (the transposed read stays coalesced);
+// blockIdx.z picks the operand, so both operands of a GEMM split in one
+// launch.
+__global__ void __launch_bounds__(256) split_kernel(const SplitOp a, const SplitOp b, int k, int kt)
 {
     __shared__ float tile[32][33];
+    const SplitOp &o = blockIdx.z == 0 ? a : b;
+    const float *__restrict__ S = o.S;
+    const int64_t lds = o.lds;
+    const int rows = o.rows, trans = o.trans;
+    uint16_t *__restrict__ out = o.out;
     const int64_t op = (int64_t)kt * 3 * kTcK; // out row pitch (elements)
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    if (r0 >= rows)
+        return;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5; // 32 x 8
     for (int i = ty; i < 32; i += 8) {
         float v = 0.f;
@@ -502,14 +517,22 @@ nm_status tc_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t kt, int npa
                        : launch_tc<3, 32>(A, B, kt, C, ldc, M, N, k_base, flags, alpha, beta, status, st);
 }
 
-nm_status tc_split(const float *S, int64_t lds, int64_t rows, int64_t k, bool trans, uint16_t *out, cudaStream_t st)
+// Splits A (rows_a x k) and, unless b_rows is 0, B (b_rows x k) in one launch.
+nm_status tc_split2(const float *A, int64_t lda, int64_t a_rows, bool a_trans, uint16_t *a_out, const float *B,
+                    int64_t ldb, int64_t b_rows, bool b_trans, uint16_t *b_out, int64_t k, cudaStream_t st)
 {
-    if (rows <= 0 || k <= 0)
+    if (k <= 0 || (a_rows <= 0 && b_rows <= 0))
         return NM_OK;
+    if (a_rows > 0x7FFFFFFF || b_rows > 0x7FFFFFFF || k > 0x7FFFFFFF)
+        return NM_ERR_SHAPE;
     const int64_t kt = (k + kTcK - 1) / kTcK;
+    const int64_t rmax = a_rows > b_rows ? a_rows : b_rows;
     // the padding columns up to kt * 64 are written as zero parts by the kernel (grid covers them)
-    const dim3 grid((unsigned)((kt * kTcK + 31) / 32), (unsigned)((rows + 31) / 32));
-    split_kernel<<<grid, 256, 0, st>>>(S, lds, (int)rows, (int)k, trans ? 1 : 0, out, (int)kt);
+    const dim3 grid((unsigned)((kt * kTcK + 31) / 32), (unsigned)((rmax + 31) / 32), b_rows > 0 ? 2u : 1u);
+    if (grid.y > 65535)
+        return NM_ERR_SHAPE;
+    const SplitOp a{A, lda, (int)a_rows, a_trans ? 1 : 0, a_out}, b{B, ldb, (int)b_rows, b_trans ? 1 : 0, b_out};
+    split_kernel<<<grid, 256, 0, st>>>(a, b, (int)k, (int)kt);
     return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }
 
@@ -618,8 +641,7 @@ nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B,
         const float *Ak = a_trans ? A + k0 * lda : A + k0;
         const float *Bk = b_trans ? B + k0 * ldb : B + k0;
         nm_status s;
-        if ((s = tc_split(Ak, lda, M, kc, a_trans, work_a, st)) != NM_OK ||
-            (!same && (s = tc_split(Bk, ldb, N, kc, b_trans, work_b, st)) != NM_OK))
+        if ((s = tc_split2(Ak, lda, M, a_trans, work_a, Bk, ldb, same ? 0 : N, b_trans, work_b, kc, st)) != NM_OK)
             return s;
         if ((s = tc_gemm_bf16(work_a, same ? work_a : work_b, (kc + kTcK - 1) / kTcK, 3, C, ldc, M, N, alpha,
                               k0 == 0 ? beta : 1.0f, status, st, flags, k0)) != NM_OK)
