@@ -388,7 +388,7 @@ nm_status nm_device_status(void *stream);
  * tiles on and below the diagonal are computed and mirrored). T == 0 writes
  * zeros (or leaves H as it is when accumulating). K must be a multiple of 32;
  * T and K at most 2^31 - 1. Workspace: X transposed, 2 K ceil(T/64)*64 bytes
- * from the stream-ordered allocator. Asynchronous on `stream`. Calls on one
+ * from the library's workspace pool. Asynchronous on `stream`. Calls on one
  * device are serialized by a lock.
  */
 nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int accumulate, void *stream);
@@ -414,14 +414,25 @@ nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, float *H, int
  * this library's kernels (the GEMMs on the tensor cores with fp32 emulated,
  * see NM_OBS_SGEMM). Workspace: 12 K^2 + 4 rows K + 4096 rows bytes, plus
  * 6144 (max(rows, K/2) + K) bytes for the GEMMs' split operands (none with
- * NM_OBS_SGEMM), taken from the stream-ordered allocator and returned before
- * the call ends. SYNCHRONOUS: returns after the result is written (NM_ERR_NOT_PD when
+ * NM_OBS_SGEMM), taken from the library's workspace pool and returned to it
+ * before the call ends (the pool keeps the memory for the next call; see
+ * nm_obs_release_workspace). SYNCHRONOUS: returns after the result is written (NM_ERR_NOT_PD when
  * the damped Hessian cannot be factorised; outputs are then unspecified).
  * Calls on one device are serialized by a lock. Pointers 16-byte aligned
  * (NM_ERR_ALIGN).
  */
 nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t rows, int64_t K, int N, int M, float percdamp,
                        unsigned flags, void *W_out_bf16, uint32_t *keep_masks, float *W_out_f32, void *stream);
+
+/*
+ * nm_obs_release_workspace -- returns to the device the memory that
+ * nm_obs_prune and nm_obs_hessian keep for their workspaces. Those calls take
+ * their workspaces from a library-owned stream-ordered pool on the current
+ * device that keeps what it has mapped between calls (mapping several GB
+ * afresh cost every call time); this trims the pool to the memory still in use
+ * by work in flight. Calls on one device are serialized by a lock.
+ */
+nm_status nm_obs_release_workspace(void);
 
 #ifdef __cplusplus
 }

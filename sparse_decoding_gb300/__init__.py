@@ -43,7 +43,7 @@ EXPORTS = ("nm_abi_version", "nm_status_str", "nm_pack_host", "nm_select", "nm_p
            "nm_spmv_f32out", "dense_gemv", "dense_gemv_f32out", "nm_spmv_stack", "dense_gemv_stack",
            "nm_device_status", "nm_spmv_noalloc", "nm_stack_plan_create", "nm_stack_plan_run",
            "nm_stack_plan_destroy", "nm_pack_swiglu", "nm_spmv_swiglu", "nm_obs_hessian", "nm_obs_prune",
-           "nm_spmv_f32out_atomic", "nm_select_pack", "nm_spmv_qkv")
+           "nm_spmv_f32out_atomic", "nm_select_pack", "nm_spmv_qkv", "nm_obs_release_workspace")
 
 
 class NmError(RuntimeError):
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         "nm_spmv_swiglu": ([p, p, p, p, i64, i64, i32, p], i32),
         "nm_obs_hessian": ([p, i64, i64, p, i32, p], i32),
         "nm_obs_prune": ([p, p, i64, i64, i32, i32, ctypes.c_float, ctypes.c_uint, p, p, p, p], i32),
+        "nm_obs_release_workspace": ([], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -396,3 +397,8 @@ def obs_prune(W: torch.Tensor, H: torch.Tensor, N: int, M: int, percdamp: float 
                               wf.data_ptr() if wf is not None else None,
                               ctypes.c_void_p(_stream(W))), "nm_obs_prune")
     return out, m, wf
+
+
+def obs_release_workspace():
+    """Return the memory the OBS calls keep for their workspaces on the current device."""
+    _check(lib().nm_obs_release_workspace(), "nm_obs_release_workspace")

@@ -200,13 +200,13 @@ __global__ void __launch_bounds__(kFacThreads, 1)
                 if (g >= gj && rw0 + 31 > j && rw0 >= 32 * g) {
                     const float ca = colA[buf][r], cb = colB[buf][r] - ca * t;
                     const float ci0 = ca * rd0, ci1 = cb * rd1;
+                    // a_rc -= ci0 xa_c + ci1 (xb_c - t xa_c), regrouped as
+                    // (ci0 - ci1 t) xa_c + ci1 xb_c: two FMAs per entry
+                    const float e0 = fmaf(-ci1, t, ci0);
 #pragma unroll
                     for (int m = 0; m < 32; ++m)
-                        if (g > gj || m > mj + 1) {
-                            const float xa = colA[buf][32 * g + m];
-                            const float xb = colB[buf][32 * g + m] - xa * t;
-                            a[m] = fmaf(-ci1, xb, fmaf(-ci0, xa, a[m]));
-                        }
+                        if (g > gj || m > mj + 1)
+                            a[m] = fmaf(-ci1, colB[buf][32 * g + m], fmaf(-e0, colA[buf][32 * g + m], a[m]));
                 }
             }
         }
@@ -506,8 +506,14 @@ cudaError_t sweep(int M, const SweepArgs &a, int i1, int bw, int grid, cudaStrea
 
 // ---- host side ----------------------------------------------------------------
 
+// Per device: the SM count and this library's workspace pool. The pool keeps
+// what it has mapped between calls (release threshold: no limit): taking a
+// workspace of several GB from a pool that returns memory at every
+// synchronisation maps it afresh on every call. nm_obs_release_workspace
+// trims it.
 struct ObsDevice {
     int sms = 0;
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_obs_mu;  // held for the whole of each call
@@ -521,6 +527,22 @@ nm_status obs_device(ObsDevice **out)
     ObsDevice &d = g_obs[dev];
     if (!d.sms && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return NM_ERR_CUDA;
+    if (!d.pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess)
+            return NM_ERR_CUDA;
+        uint64_t keep = ~0ull;
+        if (cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return NM_ERR_CUDA;
+        }
+        d.pool = p;
+    }
     *out = &d;
     return NM_OK;
 }
@@ -531,11 +553,13 @@ int grid_for(int64_t n, int sms)
     return (int)(g < 1 ? 1 : (g < cap ? g : cap));
 }
 
-// Stream-ordered workspace, released on every return path.
+// Stream-ordered workspace from the device's pool, released (to the pool) on
+// every return path.
 struct Workspace {
     cudaStream_t st;
+    cudaMemPool_t pool;
     void *p = nullptr;
-    explicit Workspace(cudaStream_t s) : st(s) {}
+    Workspace(cudaStream_t s, cudaMemPool_t mp) : st(s), pool(mp) {}
     Workspace(const Workspace &) = delete;
     Workspace &operator=(const Workspace &) = delete;
     ~Workspace()
@@ -545,7 +569,7 @@ struct Workspace {
     }
     bool alloc(size_t bytes)
     {
-        if (cudaMallocAsync(&p, bytes, st) != cudaSuccess) {
+        if (cudaMallocFromPoolAsync(&p, bytes, pool, st) != cudaSuccess) {
             p = nullptr;
             return false;
         }
@@ -667,7 +691,7 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     const size_t off_P = off_D + round256((size_t)rows * kSuper * 4);
     const size_t off_WA = off_P + round256((size_t)rows * K * 4), off_WB = off_WA + round256(wa_bytes);
     const size_t total = off_WB + round256(wb_bytes);
-    Workspace ws(st);
+    Workspace ws(st, d->pool);
     if (!ws.alloc(total))
         return NM_ERR_CUDA;
     char *base = (char *)ws.p;
@@ -764,8 +788,11 @@ extern "C" nm_status nm_obs_hessian(const void *X_bf16, int64_t T, int64_t K, fl
     nm_status s = library_status_word(&status);
     if (s != NM_OK)
         return s;
+    ObsDevice *d = nullptr;
+    if ((s = obs_device(&d)) != NM_OK)
+        return s;
     const int64_t Tp = (T + 63) / 64 * 64;
-    Workspace ws(st);
+    Workspace ws(st, d->pool);
     if (!ws.alloc((size_t)K * Tp * 2))
         return NM_ERR_CUDA;
     uint16_t *Xt = (uint16_t *)ws.p;
@@ -796,4 +823,14 @@ extern "C" nm_status nm_obs_prune(const void *W_bf16, const float *H, int64_t ro
     nm_status s = obs_prune_impl(W_bf16, H, rows, K, N, M, percdamp, flags, W_out_bf16, keep_masks, W_out_f32, st);
     cudaError_t e = cudaStreamSynchronize(st);
     return s != NM_OK ? s : (e == cudaSuccess ? NM_OK : NM_ERR_CUDA);
+}
+
+extern "C" nm_status nm_obs_release_workspace(void)
+{
+    std::lock_guard<std::mutex> lock(g_obs_mu);
+    ObsDevice *d = nullptr;
+    nm_status s = obs_device(&d);
+    if (s != NM_OK)
+        return s;
+    return cudaMemPoolTrimTo(d->pool, 0) == cudaSuccess ? NM_OK : NM_ERR_CUDA;
 }

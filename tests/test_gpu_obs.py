@@ -141,6 +141,27 @@ def test_prune_output_feeds_pack(nm):
     assert np.array_equal(pm.cpu().numpy().view(np.uint32), keep_bits)
 
 
+def test_workspace_pool_is_reused_and_released(nm):
+    # the workspace (12 K^2 + 4 rows K + ... bytes, here about 24 MB) stays in
+    # the library's pool after a call, gives the same result on reuse, and
+    # nm_obs_release_workspace returns it to the device
+    W, X, H32 = _inputs(256, 1024, 600, seed=8)
+    first = _gpu_prune(nm, W, H32, 2, 4)
+    torch.cuda.synchronize()
+    free_kept = torch.cuda.mem_get_info()[0]
+    second = _gpu_prune(nm, W, H32, 2, 4)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_kept, "a repeated call mapped new memory"
+    for a, b in zip(first, second):
+        assert np.array_equal(a, b)
+    nm.obs_release_workspace()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] - free_kept >= 12 * 1024 * 1024, "the pool kept its memory"
+    third = _gpu_prune(nm, W, H32, 2, 4)
+    for a, b in zip(first, third):
+        assert np.array_equal(a, b)
+
+
 def test_not_positive_definite_is_reported(nm):
     W = synth.weights(8, 64, seed=1)
     H = -torch.eye(64, dtype=torch.float32)
