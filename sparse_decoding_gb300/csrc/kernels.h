@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "nm_common.cuh"
 #include "nmspmv.h"
 
@@ -66,6 +68,27 @@ nm_status stack_launch_sparse(const StackOp *ops, int n_ops, int batch, uint32_t
                               const LaunchCtx &ctx);
 nm_status stack_launch_dense(const StackOp *ops, int n_ops, int batch, uint32_t *gbar, int ctas,
                              const LaunchCtx &ctx);
+
+// Launches `kern` on `st` with programmatic dependent launch: it may be
+// scheduled while the previous kernel on the stream finishes, so it must run
+// pdl_wait_upstream() (griddepcontrol.wait) before it reads or writes anything
+// earlier work on the stream touches. The chains of short dependent kernels of
+// the OBS pruning hide their launch latency this way.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- tensor-core GEMM of the OBS pruning (tc_gemm.cu) ----
 // Structure flags (coordinates of the GEMM itself: C row i, column j, k

@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(1024) obs_diag_kernel(const float *__restrict_
                                                         unsigned char *__restrict__ dead, float *__restrict__ lam)
 {
     __shared__ double part[1024];
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     double s = 0.0;
     for (int64_t j = threadIdx.x; j < K; j += blockDim.x) {
         float h = H[j * K + j];
@@ -91,6 +93,8 @@ __global__ void __launch_bounds__(1024) obs_diag_kernel(const float *__restrict_
 __global__ void obs_reverse_damp_kernel(const float *__restrict__ H, int64_t K, const float *__restrict__ lam,
                                         float *__restrict__ Hr)
 {
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     const int64_t n = K * K;
     const float l = *lam;
     for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n; p += (int64_t)gridDim.x * blockDim.x) {
@@ -151,6 +155,8 @@ __global__ void __launch_bounds__(kFacThreads, 1)
     __shared__ __align__(16) float colB[2][kFacB];
     __shared__ float rdiag[kFacB];
     constexpr int P = kFacB + 1;
+    pdl_wait_upstream();
+    pdl_launch_dependents(); // one CTA: the next kernel's CTAs may wait on the free SMs
     {
         const int r = threadIdx.x & (kFacB - 1), g = threadIdx.x >> 7, rw0 = r & ~31;
         float a[32];
@@ -280,6 +286,8 @@ __global__ void __launch_bounds__(kFacThreads, 1)
 // the flat array of L reversed; H + lam I = R R^T with R upper triangular.
 __global__ void obs_reverse_kernel(const float *__restrict__ L, int64_t n, float *__restrict__ R)
 {
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p < n; p += (int64_t)gridDim.x * blockDim.x)
         R[p] = L[n - 1 - p];
 }
@@ -324,6 +332,8 @@ __global__ void __launch_bounds__(kSweepWarps * 32, 2) obs_sweep_kernel(
     float *rinv = Ub + kObsBlock * kObsBlock;
     float *dsq = rinv + kObsBlock;
     constexpr int kQuads = kObsBlock / 4;
+    pdl_wait_upstream();
+    pdl_launch_dependents(); // a single wave (at most two CTAs per SM)
     for (int q = threadIdx.x; q < kObsBlock * kQuads; q += blockDim.x) {
         const int a = q / kQuads, c = (q % kQuads) * 4;
         float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -488,9 +498,8 @@ template <int M> cudaError_t launch_sweep(const SweepArgs &a, int i1, int bw, in
     });
     if (attr != cudaSuccess)
         return attr;
-    obs_sweep_kernel<M><<<grid, kSweepWarps * 32, kSweepSmem, st>>>(a.W, a.dead, a.P, a.X, a.rows, a.K, i1, bw, a.N,
-                                                                      a.D, a.ldD, a.Wout, a.Wout_f32, a.masks);
-    return cudaGetLastError();
+    return launch_pdl(obs_sweep_kernel<M>, dim3(grid), dim3(kSweepWarps * 32), kSweepSmem, st, a.W, a.dead, a.P, a.X,
+                      a.rows, a.K, i1, bw, a.N, a.D, a.ldD, a.Wout, a.Wout_f32, a.masks);
 }
 
 cudaError_t sweep(int M, const SweepArgs &a, int i1, int bw, int grid, cudaStream_t st)
@@ -638,8 +647,8 @@ bool chol_inv(const RowGemm &G, float *A, float *L, float *X, int64_t K, int64_t
         });
         if (attr != cudaSuccess)
             return false;
-        fac_diag_kernel<<<1, kFacThreads, kFacSmem, st>>>(A, X, K, k0, kb, not_pd);
-        return cudaGetLastError() == cudaSuccess;
+        return launch_pdl(fac_diag_kernel, dim3(1), dim3(kFacThreads), kFacSmem, st, (const float *)A, X, K, k0, kb,
+                          not_pd) == cudaSuccess;
     }
     const int64_t bm = (b0 + b1) / 2;
     const int64_t lo = b0 * kFacB, mid = bm * kFacB, hi = (b1 * kFacB < K ? b1 * kFacB : K);
@@ -707,16 +716,16 @@ nm_status obs_prune_impl(const void *W, const float *H, int64_t rows, int64_t K,
     if (cudaMemsetAsync(base + off_flag, 0, 256, st) != cudaSuccess || cudaMemsetAsync(X, 0, kk, st) != cudaSuccess ||
         cudaMemsetAsync(P, 0, (size_t)rows * K * 4, st) != cudaSuccess)
         return NM_ERR_CUDA;
-    obs_diag_kernel<<<1, 1024, 0, st>>>(H, K, percdamp, dead, lam);
-    obs_reverse_damp_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(H, K, lam, A);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_pdl(obs_diag_kernel, dim3(1), dim3(1024), 0, st, H, K, percdamp, dead, lam) != cudaSuccess ||
+        launch_pdl(obs_reverse_damp_kernel, dim3(grid_for(K * K, d->sms)), dim3(256), 0, st, H, K, (const float *)lam,
+                   A) != cudaSuccess)
         return NM_ERR_CUDA;
     if (!chol_inv(G, A, L, X, K, 0, nb, false, not_pd, st))
         return NM_ERR_CUDA;
     // A pivot that is not positive was replaced by 1, so the rest runs on
     // finite values; the flag is read once everything is queued.
-    obs_reverse_kernel<<<grid_for(K * K, d->sms), 256, 0, st>>>(L, K * K, R);
-    if (cudaGetLastError() != cudaSuccess)
+    if (launch_pdl(obs_reverse_kernel, dim3(grid_for(K * K, d->sms)), dim3(256), 0, st, (const float *)L, K * K,
+                   R) != cudaSuccess)
         return NM_ERR_CUDA;
 
     // Sweep the blocks left to right. A block starts from W0 + P U_bb, where P

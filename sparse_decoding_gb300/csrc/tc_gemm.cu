@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = m0 + warp * 32 + lane;
 
     if (nt == 0) {
+        pdl_wait_upstream();
         // no k range: C = beta C (nothing to do when beta is 1)
         if (beta != 1.0f) {
             const float zero[32] = {};
@@ -280,6 +281,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
+    pdl_wait_upstream(); // the operands and C may be the previous kernels' output
 
     if (warp == 0 && lane == 0) {
         // producer: stage i (k-tile t_lo + i / kSub, sub-slice i % kSub) goes
@@ -333,6 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_commit(smem_addr(&done_bar)); // the accumulators are complete once every MMA is done
     }
     __syncwarp();
+    pdl_launch_dependents(); // this CTA's loads are issued: the next kernel may be scheduled
     // epilogue: every warp waits for the accumulators, then reads its 32 lanes
     const bool have = wait_bounded(smem_addr(&done_bar), 0, err);
     tc_fence_after();
@@ -393,6 +396,8 @@ struct SplitOp {
 __global__ void __launch_bounds__(256) split_kernel(const SplitOp a, const SplitOp b, int k, int kt)
 {
     __shared__ float tile[32][33];
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     const SplitOp &o = blockIdx.z == 0 ? a : b;
     const float *__restrict__ S = o.S;
     const int64_t lds = o.lds;
@@ -437,6 +442,8 @@ __global__ void __launch_bounds__(256)
     transpose_bf16_kernel(const uint16_t *__restrict__ X, int T, int K, uint16_t *__restrict__ Xt, int Tp)
 {
     __shared__ uint16_t tile[32][34];
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     const int t0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int i = ty; i < 32; i += 8) {
@@ -488,9 +495,10 @@ nm_status launch_tc(const uint16_t *A, const uint16_t *B, int64_t kt, float *C, 
     const dim3 grid((unsigned)((N + kTcN - 1) / kTcN), (unsigned)((M + kTcM - 1) / kTcM));
     if (grid.y > 65535)
         return NM_ERR_SHAPE;
-    tc_gemm_kernel<NP, KW><<<grid, kTcThreads, Cfg::kSmem, st>>>(maps, C, ldc, (int)M, (int)N, (int)kt, k_base, flags,
-                                                                 alpha, beta, status);
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    return launch_pdl(tc_gemm_kernel<NP, KW>, grid, dim3(kTcThreads), Cfg::kSmem, st, maps, C, ldc, (int)M, (int)N,
+                      (int)kt, k_base, flags, alpha, beta, status) == cudaSuccess
+               ? NM_OK
+               : NM_ERR_CUDA;
 }
 
 } // namespace
@@ -532,8 +540,8 @@ nm_status tc_split2(const float *A, int64_t lda, int64_t a_rows, bool a_trans, u
     if (grid.y > 65535)
         return NM_ERR_SHAPE;
     const SplitOp a{A, lda, (int)a_rows, a_trans ? 1 : 0, a_out}, b{B, ldb, (int)b_rows, b_trans ? 1 : 0, b_out};
-    split_kernel<<<grid, 256, 0, st>>>(a, b, (int)k, (int)kt);
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    return launch_pdl(split_kernel, grid, dim3(256), 0, st, a, b, (int)k, (int)kt) == cudaSuccess ? NM_OK
+                                                                                                  : NM_ERR_CUDA;
 }
 
 nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *Xt, int64_t Tp, cudaStream_t st)
@@ -541,8 +549,9 @@ nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *X
     if (T <= 0 || K <= 0)
         return NM_OK;
     const dim3 grid((unsigned)((K + 31) / 32), (unsigned)((Tp + 31) / 32));
-    transpose_bf16_kernel<<<grid, 256, 0, st>>>(X, (int)T, (int)K, Xt, (int)Tp);
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    return launch_pdl(transpose_bf16_kernel, grid, dim3(256), 0, st, X, (int)T, (int)K, Xt, (int)Tp) == cudaSuccess
+               ? NM_OK
+               : NM_ERR_CUDA;
 }
 
 // ---- plain fp32 on the CUDA cores (the NM_OBS_SGEMM reference mode) -----------
@@ -556,6 +565,8 @@ __global__ void __launch_bounds__(256)
 {
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
+    pdl_wait_upstream();
+    pdl_launch_dependents();
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
     float acc[4][4] = {};
@@ -611,9 +622,10 @@ nm_status simt_gemm_f32(const float *A, int64_t lda, const float *B, int64_t ldb
     const dim3 grid((unsigned)((N + 63) / 64), (unsigned)((M + 63) / 64));
     if (grid.y > 65535 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || k > 0x7FFFFFFF)
         return NM_ERR_SHAPE;
-    simt_gemm_kernel<<<grid, 256, 0, st>>>(A, lda, B, ldb, b_kn ? 1 : 0, (int)M, (int)N, (int)(k > 0 ? k : 0), C,
-                                           ldc, alpha, beta);
-    return cudaGetLastError() == cudaSuccess ? NM_OK : NM_ERR_CUDA;
+    return launch_pdl(simt_gemm_kernel, grid, dim3(256), 0, st, A, lda, B, ldb, b_kn ? 1 : 0, (int)M, (int)N,
+                      (int)(k > 0 ? k : 0), C, ldc, alpha, beta) == cudaSuccess
+               ? NM_OK
+               : NM_ERR_CUDA;
 }
 
 // The k range of an emulated fp32 GEMM goes through the tensor cores in chunks
