@@ -282,6 +282,32 @@ def test_spmv_repeatable(nm):
         assert torch.equal(y, ys[0])
 
 
+@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("N,M", [(2, 4), (16, 32)])
+def test_spmv_row_and_k_shards(nm, batch, N, M):
+    """The path shards by rows (x replicated) or by K (partial sums added):
+    concatenated row shards, and the fp32 sum of K shards, meet the same bound
+    against the fp64 oracle as the unsharded product. (A row's summation order
+    follows how its row block is split over CTAs, which depends on the shard's
+    shape, so the shards are not required to repeat the unsharded bits.)"""
+    rows, K = 4096, 4096
+    _, masks, values, x, y64, S = oracle_case(rows, K, N, M, batch, seed=21, select=False)
+    m = torch.from_numpy(masks.view(np.int32)).cuda()
+    v, xd = dev(values), dev(x)
+    full = nm.spmv(m, v, xd, f32=True).cpu().numpy()
+    check_close(full, None, y64, S, "unsharded")
+    for cuts in ([0, 2048, 4096], [0, 1024, 3072, 4096], [0, 32, 4096]):
+        parts = [nm.spmv(m[a:b].contiguous(), v[a:b].contiguous(), xd, f32=True) for a, b in zip(cuts, cuts[1:])]
+        y = torch.cat(parts, dim=1).cpu().numpy()
+        check_close(y, None, y64, S, f"row shards {cuts}")
+        # two fp32 results of the same rows, each within 1e-4 S of y64
+        assert np.all(np.abs(y.astype(np.float64) - full) <= 2 * TOL * S)
+    for cut in (2048, 1024, 128):
+        ya = nm.spmv(m[:, :cut // 32].contiguous(), v[:, :cut // 2].contiguous(), xd[:, :cut].contiguous(), f32=True)
+        yb = nm.spmv(m[:, cut // 32:].contiguous(), v[:, cut // 2:].contiguous(), xd[:, cut:].contiguous(), f32=True)
+        check_close((ya + yb).cpu().numpy(), None, y64, S, f"K shards at {cut}")
+
+
 def test_spmv_empty_and_k0(nm):
     m = torch.zeros(0, 4, dtype=torch.int32, device="cuda")
     v = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
