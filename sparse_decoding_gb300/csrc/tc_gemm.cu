@@ -5,13 +5,14 @@
 //   C = alpha * A * B^T + beta * C     A: bf16 [M][k], B: bf16 [N][k] (rows
 //                                      contiguous along k), C: fp32 [M][N]
 //
-// One CTA computes a 128 x 128 tile of C: warp 0 (one thread) streams k-tiles
-// of A and B into a ring of shared-memory stages by TMA; warp 1 (one thread)
-// issues M=128, N=128, K=16 tcgen05.mma into 128-column fp32 accumulators in
-// tensor memory (four of them, see below) and releases each stage with
-// tcgen05.commit; at the end all four warps read the accumulators with
-// tcgen05.ld (warp w: rows 32w..32w+31, one row per thread), add them, and
-// write C.
+// The kernel is persistent (one CTA per SM) and computes 128 x 128 tiles of
+// C in turn: warp 0 (one thread) streams k-slices of A and B into a ring of
+// shared-memory stages by TMA; warp 1 (one thread) issues M=128, N=128, K=16
+// tcgen05.mma into 128-column fp32 accumulators in tensor memory (four of
+// them, see below) and releases each stage with tcgen05.commit; warps 2-5
+// read a finished tile's accumulators with tcgen05.ld (one row per thread),
+// add them, hand the tensor memory back to the MMA warp, and then write C --
+// so the next tile's loads and MMAs overlap the stores.
 //
 // fp32 products (the Cholesky steps and the lazy update) are emulated with
 // bf16 parts: a = a0 + a1 + a2 with a0 = bf16(a), a1 = bf16(a - a0),
@@ -54,7 +55,7 @@ namespace {
 constexpr int kTcM = 128;        // rows of C per CTA (tensor-memory lanes)
 constexpr int kTcN = 128;        // columns of C per CTA (tensor-memory columns)
 constexpr int kTcK = 64;         // k per part tile in the operand layout
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 192;  // producer, MMA issuer, four epilogue warps
 constexpr int kTcAcc = 4;        // 128-column accumulators (all 512 tensor-memory columns)
 
 // A pipeline stage holds NP part tiles of A and NP of B, each KW columns of
@@ -221,6 +222,58 @@ __device__ __forceinline__ void tc_store32(float *C, int64_t ldc, int row, int c
     }
 }
 
+// One tile of C and its 64-wide k-tiles [t_lo, t_lo + nt) (global k =
+// k_base + 64 t); nt = 0 for a tile with no k range (C = beta C). Tiles are
+// numbered row by row, columns fastest; for a lower or symmetric C only the
+// tiles on and below the diagonal are numbered (tile i of row `by` is the
+// tile with by (by + 1) / 2 <= i < (by + 1) (by + 2) / 2).
+struct TcTile {
+    int m0, n0, t_lo, nt;
+    bool mirror;
+};
+__host__ __device__ __forceinline__ bool tc_triangular(uint32_t flags) { return (flags & (kTcCLower | kTcCSym)) != 0; }
+__device__ __forceinline__ TcTile tc_tile(int tile, int tiles_n, int ktiles, int64_t k_base, uint32_t flags)
+{
+    TcTile T;
+    int bx, by;
+    if (tc_triangular(flags)) {
+        by = (int)((sqrtf(8.0f * (float)tile + 1.0f) - 1.0f) * 0.5f);
+        while ((int64_t)by * (by + 1) / 2 > tile)
+            --by;
+        while ((int64_t)(by + 1) * (by + 2) / 2 <= tile)
+            ++by;
+        bx = tile - (int)((int64_t)by * (by + 1) / 2);
+    } else {
+        bx = tile % tiles_n;
+        by = tile / tiles_n;
+    }
+    T.n0 = bx * kTcN;
+    T.m0 = by * kTcM;
+    T.mirror = (flags & kTcCSym) && bx < by;
+    int64_t lo = k_base, hi = k_base + (int64_t)ktiles * kTcK;
+    if ((flags & kTcALower) && hi > (int64_t)T.m0 + kTcM)
+        hi = (int64_t)T.m0 + kTcM;
+    if ((flags & kTcBLower) && hi > (int64_t)T.n0 + kTcN)
+        hi = (int64_t)T.n0 + kTcN;
+    if ((flags & kTcBUpper) && lo < (int64_t)T.n0)
+        lo = (int64_t)T.n0;
+    T.t_lo = lo < hi ? (int)((lo - k_base) / kTcK) : 0;
+    T.nt = lo < hi ? (int)((hi - k_base + kTcK - 1) / kTcK) - T.t_lo : 0;
+    return T;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Persistent: each CTA takes tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Warp 0 (one thread) streams the k-slices of every tile through the stage
+// ring, warp 1 (one thread) issues the MMAs, warps 2-5 are the epilogue (warp
+// w reads tensor-memory lanes 32 (w % 4) .. + 31). The epilogue copies a
+// tile's sums into registers, hands the accumulators back (acc_empty) and
+// only then writes C, so the next tile's MMAs, and the loads ahead of them,
+// overlap the stores.
 template <int NP, int KW>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, float *C, int64_t ldc, int M, int N, int ktiles,
@@ -228,51 +281,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 {
     using Cfg = TcCfg<NP, KW>;
     constexpr int S = Cfg::kStages;
-    const int n0 = blockIdx.x * kTcN, m0 = blockIdx.y * kTcM;
-    if ((flags & (kTcCLower | kTcCSym)) && blockIdx.x > blockIdx.y)
-        return;  // above the diagonal: not needed, or written by the mirror tile
-    const bool mirror = (flags & kTcCSym) && blockIdx.x < blockIdx.y;
-    // this tile's 64-wide k-tiles [t_lo, t_hi) (global k = k_base + 64 t)
-    int64_t lo = k_base, hi = k_base + (int64_t)ktiles * kTcK;
-    if ((flags & kTcALower) && hi > (int64_t)m0 + kTcM)
-        hi = (int64_t)m0 + kTcM;
-    if ((flags & kTcBLower) && hi > (int64_t)n0 + kTcN)
-        hi = (int64_t)n0 + kTcN;
-    if ((flags & kTcBUpper) && lo < (int64_t)n0)
-        lo = (int64_t)n0;
-    const int t_lo = lo < hi ? (int)((lo - k_base) / kTcK) : 0;
-    const int t_hi = lo < hi ? (int)((hi - k_base + kTcK - 1) / kTcK) : 0;
-    const int nt = t_hi - t_lo;              // uniform over the CTA
-    const int nstage = nt * Cfg::kSub;       // pipeline stages of this tile
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = m0 + warp * 32 + lane;
-
-    if (nt == 0) {
-        pdl_wait_upstream();
-        // no k range: C = beta C (nothing to do when beta is 1)
-        if (beta != 1.0f) {
-            const float zero[32] = {};
-#pragma unroll 1
-            for (int c = 0; c < kTcN; c += 32)
-                tc_store32(C, ldc, row, n0 + c, M, N, zero, alpha, beta, mirror);
-        }
-        return;
-    }
-
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
-    __shared__ __align__(8) uint64_t done_bar;
+    __shared__ __align__(8) uint64_t acc_full;   // a tile's MMAs are done
+    __shared__ __align__(8) uint64_t acc_empty;  // the epilogue has read a tile's accumulators
     __shared__ uint32_t tmem_base;
     extern __shared__ __align__(1024) uint8_t dsmem[];
     uint8_t *const tiles = dsmem + ((1024u - (smem_addr(dsmem) & 1023u)) & 1023u);
     const uint32_t tiles0 = smem_addr(tiles);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_n = (N + kTcN - 1) / kTcN;
+    const int ntiles = tc_triangular(flags) ? tiles_n * (tiles_n + 1) / 2 : tiles_n * ((M + kTcM - 1) / kTcM);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1);
             mbar_init(smem_addr(&empty_bar[s]), 1);
         }
-        mbar_init(smem_addr(&done_bar), 1);
+        mbar_init(smem_addr(&acc_full), 1);
+        mbar_init(smem_addr(&acc_empty), 4); // one arrival per epilogue warp
         fence_mbar_init();
     }
     if (warp == 2)
@@ -282,83 +309,138 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     pdl_wait_upstream(); // the operands and C may be the previous kernels' output
+    pdl_launch_dependents();
 
-    if (warp == 0 && lane == 0) {
-        // producer: stage i (k-tile t_lo + i / kSub, sub-slice i % kSub) goes
-        // to slot i % S once the MMAs of stage i - S have released it
-        int issued = 0;
-        for (int i = 0; i < nstage; ++i) {
-            const int s = i % S;
-            if (i >= S && !wait_bounded(smem_addr(&empty_bar[s]), ((i / S) - 1) & 1, err))
-                break;
-            const uint32_t fb = smem_addr(&full_bar[s]);
-            mbar_arrive_expect_tx(fb, Cfg::kStage);
-            const uint32_t sa = tiles0 + s * Cfg::kStage;
-            const int t = t_lo + i / Cfg::kSub, x0 = (i % Cfg::kSub) * KW;
+    // a wait that ran out marks the thread dead: its later waits poll once
+    bool dead = false;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (dead)
+            return mbar_try_wait(bar, parity);
+        if (!wait_bounded(bar, parity, err))
+            dead = true;
+        return !dead;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // producer: the CTA's g-th stage goes to slot g % S once the MMAs of stage g - S released it
+            uint32_t g = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const TcTile T = tc_tile(tile, tiles_n, ktiles, k_base, flags);
+                for (int i = 0; i < T.nt * Cfg::kSub; ++i, ++g) {
+                    const int s = (int)(g % S);
+                    if (g >= (uint32_t)S && !wait(smem_addr(&empty_bar[s]), ((g / S) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&full_bar[s]);
+                    mbar_arrive_expect_tx(fb, Cfg::kStage);
+                    const uint32_t sa = tiles0 + s * Cfg::kStage;
+                    const int t = T.t_lo + i / Cfg::kSub, x0 = (i % Cfg::kSub) * KW;
 #pragma unroll
-            for (int p = 0; p < NP; ++p) {
-                const int x = (t * NP + p) * kTcK + x0;
-                tma_load_2d(sa + p * Cfg::kTile, &maps.a, x, m0, fb);
-                tma_load_2d(sa + (NP + p) * Cfg::kTile, &maps.b, x, n0, fb);
-            }
-            issued = i + 1;
-        }
-        // before leaving, let the copies that may still be in flight land (bounded)
-        for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
-            if (!wait_bounded(smem_addr(&full_bar[i % S]), (i / S) & 1, err))
-                break;
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
-        uint32_t touched = 0;
-        for (int i = 0; i < nstage; ++i) {
-            const int s = i % S;
-            if (!wait_bounded(smem_addr(&full_bar[s]), (i / S) & 1, err))
-                break;
-            tc_fence_after();
-            const uint32_t sa = tiles0 + s * Cfg::kStage, sb = sa + NP * Cfg::kTile;
-            const int u = i / Cfg::kSub;
-#pragma unroll
-            for (int q = 0; q < kProducts<NP>; ++q) {
-                const int pa = (kPartA >> (2 * q)) & 3, pb = (kPartB >> (2 * q)) & 3;
-                const int a = tc_acc(u, q, NP);
-                const uint32_t acc = tmem + (uint32_t)(a * kTcN);
-#pragma unroll
-                for (int k = 0; k < Cfg::kSlices; ++k) {
-                    const uint64_t ad = smem_desc_sw<Cfg::kSwizzleBytes>(sa + pa * Cfg::kTile + k * 32);
-                    const uint64_t bd = smem_desc_sw<Cfg::kSwizzleBytes>(sb + pb * Cfg::kTile + k * 32);
-                    tc_mma_bf16(acc, ad, bd, kIdescBf16, ((touched >> a) & 1u) | (k > 0 ? 1u : 0u));
+                    for (int p = 0; p < NP; ++p) {
+                        const int x = (t * NP + p) * kTcK + x0;
+                        tma_load_2d(sa + p * Cfg::kTile, &maps.a, x, T.m0, fb);
+                        tma_load_2d(sa + (NP + p) * Cfg::kTile, &maps.b, x, T.n0, fb);
+                    }
                 }
-                touched |= 1u << a;
             }
-            tc_commit(smem_addr(&empty_bar[s])); // the stage is free once these MMAs are done
+            // before leaving, let the copies that may still be in flight land (bounded)
+            for (uint32_t i = g > (uint32_t)S ? g - S : 0; i < g; ++i)
+                if (!wait(smem_addr(&full_bar[i % S]), (i / S) & 1))
+                    break;
         }
-        tc_commit(smem_addr(&done_bar)); // the accumulators are complete once every MMA is done
-    }
-    __syncwarp();
-    pdl_launch_dependents(); // this CTA's loads are issued: the next kernel may be scheduled
-    // epilogue: every warp waits for the accumulators, then reads its 32 lanes
-    const bool have = wait_bounded(smem_addr(&done_bar), 0, err);
-    tc_fence_after();
-    const uint32_t used = tc_used(nt, NP);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer; j counts the tiles that had a k range
+            uint32_t g = 0, j = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                const TcTile T = tc_tile(tile, tiles_n, ktiles, k_base, flags);
+                if (T.nt == 0)
+                    continue;
+                if (j > 0 && !wait(smem_addr(&acc_empty), (j - 1) & 1)) // the epilogue has the last tile's sums
+                    break;
+                tc_fence_after();
+                uint32_t touched = 0;
+                for (int i = 0; i < T.nt * Cfg::kSub; ++i, ++g) {
+                    const int s = (int)(g % S);
+                    if (!wait(smem_addr(&full_bar[s]), (g / S) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = tiles0 + s * Cfg::kStage, sb = sa + NP * Cfg::kTile;
+                    const int u = i / Cfg::kSub;
+#pragma unroll
+                    for (int q = 0; q < kProducts<NP>; ++q) {
+                        const int pa = (kPartA >> (2 * q)) & 3, pb = (kPartB >> (2 * q)) & 3;
+                        const int a = tc_acc(u, q, NP);
+                        const uint32_t acc = tmem + (uint32_t)(a * kTcN);
+#pragma unroll
+                        for (int k = 0; k < Cfg::kSlices; ++k) {
+                            const uint64_t ad = smem_desc_sw<Cfg::kSwizzleBytes>(sa + pa * Cfg::kTile + k * 32);
+                            const uint64_t bd = smem_desc_sw<Cfg::kSwizzleBytes>(sb + pb * Cfg::kTile + k * 32);
+                            tc_mma_bf16(acc, ad, bd, kIdescBf16, ((touched >> a) & 1u) | (k > 0 ? 1u : 0u));
+                        }
+                        touched |= 1u << a;
+                    }
+                    tc_commit(smem_addr(&empty_bar[s])); // the stage is free once these MMAs are done
+                }
+                tc_commit(smem_addr(&acc_full)); // the tile's accumulators are complete once its MMAs are done
+                ++j;
+            }
+        }
+    } else {
+        // epilogue: warp w handles tensor-memory lanes (rows) 32 (w % 4) .. + 31
+        const int qw = warp & 3;
+        uint32_t j = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const TcTile T = tc_tile(tile, tiles_n, ktiles, k_base, flags);
+            const int row = T.m0 + qw * 32 + lane;
+            if (T.nt == 0) {
+                // no k range: C = beta C (nothing to do when beta is 1)
+                if (beta != 1.0f) {
+                    const float zero[32] = {};
 #pragma unroll 1
-    for (int c = 0; c < kTcN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, r);
-#pragma unroll 1
-        for (int a = 1; a < kTcAcc; ++a) {
-            if (!(used & (1u << a)))
+                    for (int c = 0; c < kTcN; c += 32)
+                        tc_store32(C, ldc, row, T.n0 + c, M, N, zero, alpha, beta, T.mirror);
+                }
                 continue;
-            uint32_t r2[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * kTcN + c), r2);
+            }
+            const bool have = wait(smem_addr(&acc_full), j & 1);
+            tc_fence_after();
+            // the accumulators that received a product, added in index order
+            const uint32_t used = tc_used(T.nt, NP);
+            float v[4][32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r2[j]));
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(c * 32), r);
+#pragma unroll 1
+                for (int a = 1; a < kTcAcc; ++a) {
+                    if (!(used & (1u << a)))
+                        continue;
+                    uint32_t r2[32];
+                    tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + (uint32_t)(a * kTcN + c * 32), r2);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    v[c][e] = have ? __uint_as_float(r[e]) : 0.0f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&acc_empty)); // the MMAs of the next tile may start
+            ++j;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tc_store32(C, ldc, row, T.n0 + 32 * c, M, N, v[c], alpha, beta, T.mirror);
         }
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            v[j] = have ? __uint_as_float(r[j]) : 0.0f;
-        tc_store32(C, ldc, row, n0 + c, M, N, v, alpha, beta, mirror);
     }
     tc_fence_before();
     __syncthreads();
@@ -492,9 +574,18 @@ nm_status launch_tc(const uint16_t *A, const uint16_t *B, int64_t kt, float *C, 
     if ((s = encode_operand<KW>(&maps.a, A, M, pitch)) != NM_OK ||
         (s = encode_operand<KW>(&maps.b, B, N, pitch)) != NM_OK)
         return s;
-    const dim3 grid((unsigned)((N + kTcN - 1) / kTcN), (unsigned)((M + kTcM - 1) / kTcM));
-    if (grid.y > 65535)
+    // persistent: one CTA per SM (its shared memory allows no second), or one per tile
+    const int64_t tn = (N + kTcN - 1) / kTcN;
+    const int64_t ntiles = tc_triangular(flags) ? tn * (tn + 1) / 2 : tn * ((M + kTcM - 1) / kTcM);
+    if (ntiles > 0x7FFFFFFF)
         return NM_ERR_SHAPE;
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return NM_ERR_CUDA;
+    if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return NM_ERR_CUDA;
+    const dim3 grid((unsigned)(ntiles < sms[dev] ? ntiles : sms[dev]));
     return launch_pdl(tc_gemm_kernel<NP, KW>, grid, dim3(kTcThreads), Cfg::kSmem, st, maps, C, ldc, (int)M, (int)N,
                       (int)kt, k_base, flags, alpha, beta, status) == cudaSuccess
                ? NM_OK
