@@ -119,6 +119,9 @@ nm_status tc_gemm_f32(const float *A, int64_t lda, bool a_trans, const float *B,
 size_t tc_operand_bytes(int64_t rows, int64_t k, bool emulated);
 // Xt [K][Tp] = X^T (bf16 X [T][K]), zero in columns T .. Tp.
 nm_status tc_transpose_bf16(const uint16_t *X, int64_t T, int64_t K, uint16_t *Xt, int64_t Tp, cudaStream_t st);
+// The same product for small shapes (32 x 32 tiles, double-buffered k steps).
+nm_status simt_small_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
+                         int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st);
 // The same product in plain fp32 on the CUDA cores (b_kn: B stored k x N).
 nm_status simt_gemm_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
                         int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st);

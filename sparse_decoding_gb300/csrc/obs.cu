@@ -36,10 +36,11 @@
 //   5. the lazy update P += D R, in two levels: the rest of the current
 //      1024-column superblock after each block, every later column once per
 //      superblock (one GEMM with k up to 1024).
-// Every GEMM runs on this library's tensor-core GEMM (tc_gemm.cu): fp32
+// The GEMMs run on this library's tensor-core GEMM (tc_gemm.cu): fp32
 // emulated by three bf16 parts per operand and the six products of order up
-// to 2, accumulated in fp32 in tensor memory; with NM_OBS_SGEMM, plain fp32 on
-// the CUDA cores instead. The Hessian is one bf16 pass (its products are exact).
+// to 2, accumulated in fp32 in tensor memory; the smallest ones (up to 256^3),
+// and all of them with NM_OBS_SGEMM, in plain fp32 on the CUDA cores. The
+// Hessian is one bf16 pass (its products are exact).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -590,7 +591,11 @@ size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Row-major fp32 GEMMs on K-strided buffers: on the tensor cores with fp32
 // emulated by bf16 parts (wa, wb: the split operands' workspace), or plain
-// fp32 on the CUDA cores.
+// fp32 on the CUDA cores -- always with NM_OBS_SGEMM, and for products of at
+// most kSmallMax multiply-adds (up to 256^3: the leaves of the Cholesky
+// recursion), where the small-shape kernel takes 6-10 us against 14-16 us
+// for the operand split and the tensor-core launch.
+constexpr int64_t kSmallMax = (int64_t)1 << 24;
 struct RowGemm {
     bool plain;
     int64_t ld;
@@ -605,6 +610,8 @@ struct RowGemm {
     {
         if (plain)
             return simt_gemm_f32(A, lda, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, st) == NM_OK;
+        if (M * N * k <= kSmallMax)
+            return simt_small_f32(A, lda, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, st) == NM_OK;
         return tc_gemm_f32(A, lda, false, B, ldb, b_kn, M, N, k, C, ldc, alpha, beta, wa, wb, status, st, tri) ==
                NM_OK;
     }

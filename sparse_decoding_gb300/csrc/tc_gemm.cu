@@ -705,6 +705,91 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The same product for small shapes (the leaves of the Cholesky recursion,
+// where one split launch and one tensor-core launch cost more than the
+// arithmetic): 32 x 32 outputs per CTA of 256 threads (four consecutive
+// columns each), k in steps of 32 through shared memory, the next step's
+// operands loaded into registers while the current one is multiplied.
+__global__ void __launch_bounds__(256)
+    simt_small_kernel(const float *__restrict__ A, int64_t lda, const float *__restrict__ B, int64_t ldb, int b_kn,
+                      int M, int N, int k, float *C, int64_t ldc, float alpha, float beta)
+{
+    __shared__ float As[32][33];                 // [k][m]
+    __shared__ __align__(16) float Bs[32][36];   // [k][n]
+    pdl_wait_upstream();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x;
+    const int m0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
+    const int r = tid >> 3, c = (tid & 7) * 4;   // this thread's output row and first column
+    const int li = tid >> 3, lj = (tid & 7) * 4; // this thread's four elements of each loaded tile
+    float ra[4], rb[4];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = m0 + li, kk = k0 + lj + e;
+            ra[e] = (m < M && kk < k) ? A[(int64_t)m * lda + kk] : 0.f;
+            if (b_kn) {
+                const int kr = k0 + li, n = n0 + lj + e; // B is k x N
+                rb[e] = (kr < k && n < N) ? B[(int64_t)kr * ldb + n] : 0.f;
+            } else {
+                const int n = n0 + li; // B is N x k
+                rb[e] = (n < N && kk < k) ? B[(int64_t)n * ldb + kk] : 0.f;
+            }
+        }
+    };
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (k > 0)
+        load(0);
+    for (int k0 = 0; k0 < k; k0 += 32) {
+        __syncthreads(); // the previous step's reads of the tiles are done
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            As[lj + e][li] = ra[e];
+            if (b_kn)
+                Bs[li][lj + e] = rb[e];
+            else
+                Bs[lj + e][li] = rb[e];
+        }
+        __syncthreads();
+        if (k0 + 32 < k)
+            load(k0 + 32);
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            const float a = As[kk][r];
+            const float4 b = *reinterpret_cast<const float4 *>(&Bs[kk][c]);
+            acc[0] = fmaf(a, b.x, acc[0]);
+            acc[1] = fmaf(a, b.y, acc[1]);
+            acc[2] = fmaf(a, b.z, acc[2]);
+            acc[3] = fmaf(a, b.w, acc[3]);
+        }
+    }
+    const int m = m0 + r;
+    if (m < M) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = n0 + c + e;
+            if (n < N) {
+                float *d = C + (int64_t)m * ldc + n;
+                *d = beta != 0.f ? fmaf(beta, *d, alpha * acc[e]) : alpha * acc[e];
+            }
+        }
+    }
+}
+
+nm_status simt_small_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
+                         int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st)
+{
+    if (M <= 0 || N <= 0)
+        return NM_OK;
+    const dim3 grid((unsigned)((N + 31) / 32), (unsigned)((M + 31) / 32));
+    if (grid.y > 65535 || M > 0x7FFFFFFF || N > 0x7FFFFFFF || k > 0x7FFFFFFF)
+        return NM_ERR_SHAPE;
+    return launch_pdl(simt_small_kernel, grid, dim3(256), 0, st, A, lda, B, ldb, b_kn ? 1 : 0, (int)M, (int)N,
+                      (int)(k > 0 ? k : 0), C, ldc, alpha, beta) == cudaSuccess
+               ? NM_OK
+               : NM_ERR_CUDA;
+}
+
 nm_status simt_gemm_f32(const float *A, int64_t lda, const float *B, int64_t ldb, bool b_kn, int64_t M, int64_t N,
                         int64_t k, float *C, int64_t ldc, float alpha, float beta, cudaStream_t st)
 {
