@@ -6,9 +6,11 @@
 // steps 2-3). Each mask word has exactly 16 set bits, so every word takes the
 // same 16 steps: find a set bit (its position is the column of the next kept
 // value), clear it, multiply-accumulate. The pages walk from the least
-// significant bit; here the walk runs from the most significant bit down,
-// which visits the same (column, value) pairs in reverse order with a
-// shorter dependency chain (bfind, clear) -- the product is the same sum.
+// significant bit; here each word is walked from both ends at once (the
+// highest remaining set bit gives values 15..8, the lowest values 0..7), two
+// independent 8-step dependency chains over the same (column, value) pairs --
+// the product is the same sum. Words whose bytes all hold four set bits (2:4,
+// 4:8) take their columns from byte tables instead.
 //
 // Main kernel (K % 128 == 0): the stream-K TMA driver of streamk.cuh with
 // units of 32 rows x 128 columns (4 mask words per row). A stage is filled by
@@ -18,8 +20,8 @@
 // Lane i of a warp owns row i of the unit, so all 32 lanes read x inside the
 // same 32-column window. At batch 1 lane j holds column j of that window in a
 // register and the gather is a warp shuffle; at batch > 1 the window is
-// converted to fp32 [column][batch] in shared memory and the gather is one
-// conflict-free shared load per column.
+// transposed to bf16 [column][batch] in shared memory and the gather is one
+// conflict-free shared load per column (all batch rows).
 //
 // Fallback kernel (any K % 32 == 0): the same lane-per-row walk with plain
 // loads from global memory.
