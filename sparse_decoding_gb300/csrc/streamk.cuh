@@ -10,10 +10,11 @@
 // are requested before the kernel waits for the previous kernel (programmatic
 // dependent launch), x only after.
 //
-// A row block split between warps of one CTA is finished by the warp that
-// arrives last (a shared-memory counter); one split between CTAs by the CTA
-// that arrives last (a counter in the scratch). Partial sums are added in a
-// fixed order, so results repeat bit for bit, and nobody waits for anybody.
+// A row block split between warps of one CTA is finished, after the CTA's
+// barrier, by the warp that holds its last part (it adds the parts in warp
+// order); one split between CTAs by the CTA that arrives last (a counter in
+// the scratch). Partial sums are added in a fixed order, so results repeat
+// bit for bit.
 //
 // A unit policy `Pol` supplies the stage layout and the per-unit arithmetic:
 //   Pol::kCols            columns per unit
