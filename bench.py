@@ -712,6 +712,16 @@ def run_suite(args):
             shp = synth.MODELS[model]
             res["workload"] = (f"{model}-shaped decode-token linear stack: {stack.layers} layers x ("
                                + ", ".join(f"{n} {shp[n][0]}x{shp[n][1]}" for n in synth.MATRICES) + ")")
+            # the CPU oracle beside it: one layer's sampled rows, scaled to the stack (extrapolated)
+            N0, M0 = pats[0]
+            sample = build_oracle_sample(model, N0, M0, 1, row_frac=1 / 64)
+            t_tok = min(time_oracle_token(sample, stack.layers)[1] for _ in range(2))
+            cores = cpu_cores_available()
+            t_all = time_oracle_token_threads(sample, stack.layers, cores)
+            res["cpu_oracle_extrapolated"] = {
+                "us_per_token": round(t_tok * 1e6, 1), "cores": 1,
+                "all_cores_us_per_token": round(t_all * 1e6, 1), "all_cores": cores,
+                "sample": sample_desc(sample, stack.layers, N0, M0, 1) + " (extrapolated from one layer)"}
             out["models"][model] = res
             del stack
             torch.cuda.empty_cache()
