@@ -10,7 +10,7 @@
 // highest remaining set bit gives values 15..8, the lowest values 0..7), two
 // independent 8-step dependency chains over the same (column, value) pairs --
 // the product is the same sum. Words whose bytes all hold four set bits (2:4,
-// 4:8) take their columns from byte tables instead.
+// 4:8) take their columns from byte tables instead (batch 1 and 2).
 //
 // Main kernel (K % 128 == 0): the stream-K TMA driver of streamk.cuh with
 // units of 32 rows x 128 columns (4 mask words per row). A stage is filled by
@@ -19,9 +19,10 @@
 //
 // Lane i of a warp owns row i of the unit, so all 32 lanes read x inside the
 // same 32-column window. At batch 1 lane j holds column j of that window in a
-// register and the gather is a warp shuffle; at batch > 1 the window is
-// transposed to bf16 [column][batch] in shared memory and the gather is one
-// conflict-free shared load per column (all batch rows).
+// register and the gather is a warp shuffle (at batch 2 the same, the two
+// batch rows as one bf16 pair, for byte-regular words); otherwise the window
+// is transposed to bf16 [column][batch] in shared memory and the gather is
+// one conflict-free shared load per column (all batch rows).
 //
 // Fallback kernel (any K % 32 == 0): the same lane-per-row walk with plain
 // loads from global memory.
@@ -179,6 +180,65 @@ __device__ __forceinline__ bool walk_unit_b1_lut(const uint32_t (&m)[4], const u
     return true;
 }
 
+// Batch 2, byte-regular words: the byte tables give each kept value's
+// column as a shuffle source lane, as at batch 1. Lane j holds column
+// 32 q + j of the unit's x slice for every batch row, as bf16 pairs (rows 2h
+// and 2h + 1 in xq[h]), so one shuffle gathers two batch rows and no window
+// is transposed. Returns false, having accumulated nothing, if any lane of the
+// warp holds a word that is not byte-regular.
+template <int B>
+__device__ __forceinline__ bool walk_unit_bn_lut(const uint32_t (&m)[4], const uint32_t (&v)[4][8],
+                                                 const uint8_t *sx, const uint32_t *lut, int lane,
+                                                 float (&acc)[4][B])
+{
+    constexpr int H = (B + 1) / 2; // registers of bf16 pairs per column
+    uint32_t ent[4][4];
+    uint32_t flags = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            ent[q][b] = lut[b * 256 + ((m[q] >> (8 * b)) & 0xFFu)];
+            flags |= ent[q][b];
+        }
+    if (!__all_sync(0xFFFFFFFFu, (flags & kIrregular) == 0))
+        return false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t xq[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const uint32_t lo = *(const uint16_t *)(sx + (2 * h) * (kSpCols * 2) + (32 * q + lane) * 2);
+            const uint32_t hi =
+                2 * h + 1 < B ? *(const uint16_t *)(sx + (2 * h + 1) * (kSpCols * 2) + (32 * q + lane) * 2) : 0u;
+            xq[h] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t e = ent[q][b];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t wp = v[q][2 * b + (k >> 1)]; // values 4b + k: pair k / 2, half k % 2
+                const int src = (int)(e >> (8 * k));          // a shuffle reads the low 5 bits
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const uint32_t xv = __shfl_sync(0xFFFFFFFFu, xq[h], src);
+                    if (k & 1) {
+                        acc[q][2 * h] = fma_bf16<1, 0>(wp, xv, acc[q][2 * h]);
+                        if (2 * h + 1 < B)
+                            acc[q][(2 * h + 1) % B] = fma_bf16<1, 1>(wp, xv, acc[q][(2 * h + 1) % B]);
+                    } else {
+                        acc[q][2 * h] = fma_bf16<0, 0>(wp, xv, acc[q][2 * h]);
+                        if (2 * h + 1 < B)
+                            acc[q][(2 * h + 1) % B] = fma_bf16<0, 1>(wp, xv, acc[q][(2 * h + 1) % B]);
+                    }
+                }
+            }
+        }
+    }
+    return true;
+}
+
 // x slice of one unit, bf16 [B][128] (as copied) -> bf16 [128][BP] in the
 // warp's window: the batch rows of a column side by side, two per 32-bit word.
 template <int B>
@@ -319,6 +379,16 @@ struct SparseUnit {
             }
             walk_unit_b1(r.m, r.v, xs, lane, acc);
         } else {
+            // batch 2: byte tables with shuffled x; wider batches need a shuffle
+            // per bf16 pair of batch rows per kept value, which costs more than
+            // the walk's shared-memory window (batch 4 even, batch 8 -12%)
+            if constexpr (B <= 2) {
+                if (stt.try_lut) {
+                    if (walk_unit_bn_lut<B>(r.m, r.v, xs, (const uint32_t *)ps, lane, acc))
+                        return;
+                    stt.try_lut = false;
+                }
+            }
             transpose_x_bf16<B>(xs, xf, lane);
             __syncwarp();
             walk_unit_bn<B>(r.m, r.v, xf, lane, acc);
