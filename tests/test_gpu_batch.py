@@ -1,7 +1,8 @@
 """GPU parity of the decode SpMV at batch 2..8 against the CPU oracle.
 
-At batch > 1 each warp walks its units with x from a bf16 [column][batch]
-window (the byte tables serve batch 1 only). The shapes cover: row blocks of
+At batch 2, byte-regular words take the byte tables with both batch rows
+shuffled as one bf16 pair; otherwise each warp walks its units with x from a
+bf16 [column][batch] window in shared memory. The shapes cover: row blocks of
 one CTA, partial row blocks (rows not a multiple of 32), row blocks whose K is
 split over many CTAs (the fix-up across CTAs), every batch size, matrices
 mixing 2:4 rows with 4:8, 8:16 and 16:32 rows, activations holding Inf and
@@ -60,7 +61,7 @@ def test_batch_mixed_patterns(nm, batch):
     check_close(y32, ybf, y64, S, f"mixed units b{batch}")
 
 
-@pytest.mark.parametrize("batch", [1, 4, 8])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
 def test_nonfinite_x_reaches_only_rows_that_keep_its_column(nm, batch):
     """x holding +Inf, -Inf and NaN at a few columns. The format's sum has a
     term for kept values only, so such a column reaches just the rows that keep
@@ -96,7 +97,7 @@ def test_nonfinite_x_reaches_only_rows_that_keep_its_column(nm, batch):
                     f"finite rows b{batch}")
 
 
-@pytest.mark.parametrize("batch", [4, 8])
+@pytest.mark.parametrize("batch", [2, 4, 8])
 def test_batch_exact_dyadic(nm, batch):
     """Dyadic weights, small-integer x: every partial sum is exact in fp32, so
     the result equals the fp64 one exactly."""
@@ -110,10 +111,11 @@ def test_batch_exact_dyadic(nm, batch):
         np.testing.assert_array_equal(ybf, bf16_round_np(y64.astype(np.float32)))
 
 
-def test_batch_repeatable(nm):
+@pytest.mark.parametrize("batch", [2, 8])
+def test_batch_repeatable(nm, batch):
     """Each warp's order of products is fixed and the fix-up adds parts in
     warp and CTA order: repeated calls give identical bits."""
-    _, masks, values, x, _, _ = oracle_case(4096, 14336, 2, 4, 8, seed=9, select=False)
+    _, masks, values, x, _, _ = oracle_case(4096, 14336, 2, 4, batch, seed=9, select=False)
     m = torch.from_numpy(masks.view(np.int32)).cuda()
     v, xd = dev(values), dev(x)
     ys = [nm.spmv(m, v, xd, f32=True) for _ in range(3)]
