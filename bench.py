@@ -741,7 +741,7 @@ def run_ours(args):
     patterns = [head]
     if not args.no_variants:
         patterns += [p for p in synth.PATTERNS if p != head]
-    batches = [args.batch] + ([] if args.no_variants or args.batch == 4 else [4])
+    batches = [args.batch] + ([] if args.no_variants else [b for b in (2, 4, 8) if b != args.batch])
     stack = Stack(nm, args.model, patterns, batches, args.layers, keep_dense=True)
     layers = stack.layers
     B = args.batch
@@ -824,19 +824,21 @@ def run_ours(args):
         # every pattern at the headline batch (the pages: the same traffic for all four)
         for pat in patterns[1:]:
             variants[f"{pat[0]}:{pat[1]} batch {B}"] = variant_entry(time_plan(stack.sparse_ops(pat, B), B), B)
-        # batch 4, with the dense references at batch 4
-        if 4 in stack.io and B != 4:
-            t4 = time_plan(stack.sparse_ops(head, 4), 4)
-            dense4_ops = stack.dense_ops(4)
-            d4 = {"hand_written": time_plan(dense4_ops, 4, dense=True)}
+        # batch 2, 4 and 8, each with the dense references at that batch
+        for bb in (2, 4, 8):
+            if bb not in stack.io or bb == B:
+                continue
+            tb = time_plan(stack.sparse_ops(head, bb), bb)
+            dense_ops = stack.dense_ops(bb)
+            db = {"hand_written": time_plan(dense_ops, bb, dense=True)}
 
-            def cublas4():
-                for op in dense4_ops:
+            def cublas_b(dense_ops=dense_ops):
+                for op in dense_ops:
                     torch.mm(op["x"], op["W"].t(), out=op["y"])
-            g = capture(cublas4)
-            d4["cublas"], _ = time_graph(g, args.steps, min(args.warmup, 10), world)
+            g = capture(cublas_b)
+            db["cublas"], _ = time_graph(g, args.steps, min(args.warmup, 10), world)
             del g
-            variants[f"{head[0]}:{head[1]} batch 4"] = variant_entry(t4, 4, d4)
+            variants[f"{head[0]}:{head[1]} batch {bb}"] = variant_entry(tb, bb, db)
         # q, k and v stored apart (three buffers per qkv linear)
         rq, rk = synth.QKV_SPLIT[args.model]
         for b in sorted({B} | ({4} if 4 in stack.io else set())):
