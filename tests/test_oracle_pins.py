@@ -314,6 +314,26 @@ def test_spmv_nan_propagates_to_its_row_only():
     assert np.isnan(y[0, 1]) and not np.isnan(y[0, [0, 2, 3]]).any()
 
 
+def test_spmv_nonfinite_x_is_the_dense_product():
+    """The oracle is the dense product over the pruned W (IEEE arithmetic):
+    an Inf in x_j times a pruned zero gives NaN in every row that prunes
+    column j, and rows that keep it get +-Inf. This is why the GPU test of
+    non-finite activations builds the format's kept-terms-only expectation
+    from the oracle run with that entry zeroed, not from this value."""
+    rows, K = 64, 128
+    W = to_bits(synth.nm_structured(rows, K, 2, 4, seed=17))
+    c = 9
+    x = to_bits(synth.activations(1, K, seed=17))
+    x[0, c] = 0x7F80  # +Inf
+    y, _ = oracle.spmv_f64(W, x)
+    keeps = W[:, c] != 0
+    assert keeps.any() and (~keeps).any()
+    assert np.all(np.isnan(y[0][~keeps]))
+    w = bits_to_f64(W[keeps, c])
+    np.testing.assert_array_equal(np.sign(y[0][keeps]), np.sign(w))
+    assert np.all(np.isinf(y[0][keeps]))
+
+
 def test_packed_path_equals_dense_path():
     rows, K = 33, 1024
     W = to_bits(synth.nm_structured(rows, K, 16, 32, seed=16))
